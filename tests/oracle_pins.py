@@ -1,0 +1,285 @@
+"""Pins of the CPU oracle to facts outside itself.
+
+Each ``check_*`` function takes an oracle module (the real one, or a mutant
+built by ``tests/test_oracle_mutations.py``) and raises AssertionError when the
+oracle disagrees with: the hand-worked golden example, brute force from the
+raw bytes on tiny shapes, library routines (torch rms_norm / silu / round /
+einsum), closed forms, or invariants.  None of them re-types the oracle's own
+formula: every check reaches the expected value by another route.
+"""
+
+from __future__ import annotations
+
+import os
+import random
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def read_golden(name: str) -> dict:
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            out.setdefault(key, []).append(rest.split())
+    return out
+
+
+def hand_case(fmt: str):
+    """(wbuf uint8, x bf16 bits, expected dict) of the hand-worked example."""
+    g = read_golden("hand_1x32.txt")
+    N, K = int(g["N"][0][0]), int(g["K"][0][0])
+    rows = [bytes.fromhex(g[f"{fmt}_row0"][0][0]), bytes.fromhex(g[f"{fmt}_row1"][0][0])]
+    rows += [bytes.fromhex(g[f"{fmt}_rest"][0][0])] * (N - 2)
+    scales = np.array([float(v) for v in g["scales"][0]], dtype="<f4")
+    wbuf = np.frombuffer(b"".join(rows) + scales.tobytes(), dtype=np.uint8).copy()
+    x = torch.tensor([[float(v) for v in g["x"][0]]], dtype=torch.float32).to(torch.bfloat16)
+    assert torch.equal(x.float(), torch.tensor([[float(v) for v in g["x"][0]]])), "x not exact in bf16"
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    exp = {
+        "N": N, "K": K, "G": int(g["G"][0][0]),
+        "q": np.array([int(v) for v in g["q"][0]], dtype=np.int64),
+        "s": float(g["s"][0][0]),
+        "acc": np.array([int(v) for v in g["acc"][0]], dtype=np.int64),
+        "y": np.array([float(v) for v in g["y"][0]], dtype=np.float32),
+    }
+    return wbuf, xb, exp
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+def check_hand_example(O):
+    for fmt in ("w4a8", "w6a8"):
+        wbuf, xb, e = hand_case(fmt)
+        r = O.forward(fmt, "none", e["N"], e["K"], e["G"], wbuf, x=xb)
+        assert np.array_equal(r["q"][0], e["q"]), (fmt, r["q"][0])
+        assert r["s"][0] == e["s"], (fmt, r["s"])
+        assert np.array_equal(r["acc"][0, :, 0], e["acc"]), (fmt, r["acc"][0, :, 0])
+        assert np.array_equal(r["y"][0], e["y"]), (fmt, r["y"][0])
+
+
+def _bitstream_codes(fmt, N, K, wbuf):
+    """Codes read as an LSB-first bit stream per row (independent of the oracle)."""
+    b = {"w4a8": 4, "w6a8": 6}[fmt]
+    rb = K * b // 8
+    out = np.zeros((N, K), dtype=np.int64)
+    for n in range(N):
+        big = int.from_bytes(bytes(wbuf[n * rb:(n + 1) * rb]), "little")
+        for k in range(K):
+            out[n, k] = (big >> (b * k)) & ((1 << b) - 1)
+    return out
+
+
+def _bruteforce_y(fmt, N, K, G, wbuf, q, s):
+    """y from raw bytes by pure-Python loops over the dequantised weight."""
+    b = {"w4a8": 4, "w6a8": 6}[fmt]
+    codes = _bitstream_codes(fmt, N, K, wbuf)
+    off = N * K * b // 8
+    scale_bytes = bytes(wbuf[off:off + N * (K // G) * 4])
+    sw = [[float(np.frombuffer(scale_bytes[4 * (n * (K // G) + gg):4 * (n * (K // G) + gg) + 4], "<f4")[0])
+           for gg in range(K // G)] for n in range(N)]
+    M = q.shape[0]
+    y = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            tot = 0.0
+            for k in range(K):
+                w = sw[n][k // G] * float(int(codes[n, k]) - (1 << (b - 1)))
+                tot += (s[m] * float(q[m, k])) * w
+            y[m, n] = tot
+    return y
+
+
+def check_file_layout(O, seed=1):
+    rng = np.random.default_rng(seed)
+    for fmt in ("w4a8", "w6a8"):
+        for (N, K, G) in ((3, 32, 32), (5, 64, 32), (2, 128, 64)):
+            nb = N * K * {"w4a8": 4, "w6a8": 6}[fmt] // 8
+            wbuf = np.concatenate([rng.integers(0, 256, nb, dtype=np.uint8),
+                                   rng.uniform(0.1, 1, N * (K // G)).astype("<f4").view(np.uint8)])
+            codes, sw = O.unpack_file(fmt, N, K, G, wbuf)
+            assert np.array_equal(codes, _bitstream_codes(fmt, N, K, wbuf)), fmt
+            assert np.array_equal(sw.reshape(-1).view(np.uint8), wbuf[nb:]), fmt
+            assert np.array_equal(O.pack_file(fmt, codes, sw), wbuf), fmt
+
+
+def check_forward_bruteforce(O, seed=2):
+    rng = random.Random(seed)
+    for fmt in ("w4a8", "w6a8"):
+        for (N, K, G) in ((16, 32, 32), (16, 64, 32), (32, 128, 64), (16, 128, 32)):
+            M = rng.randint(1, 8)
+            gen = torch.Generator().manual_seed(rng.randint(0, 10**6))
+            x = torch.randn(M, K, generator=gen).to(torch.bfloat16)
+            nb = N * K * {"w4a8": 4, "w6a8": 6}[fmt] // 8
+            codes = torch.randint(0, 256, (nb,), generator=gen, dtype=torch.uint8).numpy()
+            sw = torch.empty(N * (K // G)).uniform_(0.01, 0.02, generator=gen).numpy().astype("<f4")
+            wbuf = np.concatenate([codes, sw.view(np.uint8)])
+            r = O.forward(fmt, "none", N, K, G, wbuf, x=bits_of(x))
+            yb = _bruteforce_y(fmt, N, K, G, wbuf, r["q"], r["s"])
+            assert np.allclose(r["y64"], yb, rtol=1e-12, atol=1e-12 * np.abs(yb).max()), (fmt, N, K, G)
+
+
+def check_quantize(O, seed=3):
+    # library route: torch fp32 division and torch.round (ties to even) for the fp32 recipe
+    gen = torch.Generator().manual_seed(seed)
+    x = (torch.randn(6, 96, generator=gen) * 3).to(torch.bfloat16).float()
+    x[2] = 0.0
+    x[3] = 0.0
+    x[3, 17] = -0.75
+    q, s, v = O.quantize_rows(x.double().numpy(), fp32=True)
+    amax = x.abs().amax(dim=1)
+    st = amax / 127.0
+    qt = torch.clamp(torch.round(x / st[:, None]), -127, 127)
+    qt[2] = 0
+    assert np.array_equal(q, qt[[0, 1, 2, 3, 4, 5]].numpy().astype(np.int64)), "fp32 recipe"
+    assert s[2] == 0 and np.all(q[2] == 0), "zero row"
+    assert q[3, 17] == -127 and np.count_nonzero(q[3]) == 1, "single nonzero"
+    # fp64 route: properties that hold for any correct symmetric RNE quantiser
+    a = np.random.default_rng(seed).normal(size=(5, 200)) * np.array([1, 10, 1e-3, 5, 1])[:, None]
+    q, s, v = O.quantize_rows(a, fp32=False)
+    for m in range(5):
+        assert np.isclose(s[m] * 127, np.abs(a[m]).max(), rtol=1e-15)
+        assert np.abs(q[m]).max() == 127
+        assert np.all(np.abs(q[m] - a[m] / s[m]) <= 0.5 + 1e-12)
+    # ties go to even
+    t = np.array([[127.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5]])
+    q, _, _ = O.quantize_rows(t, fp32=False)
+    assert list(q[0]) == [127, 0, 2, 2, 0, -2, -2, 126]
+
+
+def check_prologues(O, seed=4):
+    gen = torch.Generator().manual_seed(seed)
+    M, K = 3, 256
+    x = torch.randn(M, K, generator=gen).to(torch.bfloat16)
+    gamma = torch.empty(K).uniform_(0.5, 1.5, generator=gen)
+    a = O.prologue("rmsnorm", x=bits_of(x), gamma=gamma.numpy(), eps=1e-6)
+    ref = torch.nn.functional.rms_norm(x.double(), (K,), weight=gamma.double(), eps=1e-6)
+    assert np.allclose(a, ref.numpy(), rtol=1e-13, atol=0), "rmsnorm vs torch rms_norm"
+    g = torch.randn(M, K, generator=gen).to(torch.bfloat16)
+    u = torch.randn(M, K, generator=gen).to(torch.bfloat16)
+    a = O.prologue("swiglu", gate=bits_of(g), up=bits_of(u))
+    ref = torch.nn.functional.silu(g.double()) * u.double()
+    assert np.allclose(a, ref.numpy(), rtol=1e-13, atol=1e-300), "swiglu vs torch silu"
+    a = O.prologue("none", x=bits_of(x))
+    assert np.array_equal(a, x.double().numpy())
+
+
+def check_closed_forms(O, seed=5):
+    rng = np.random.default_rng(seed)
+    fmt, N, K, G = "w4a8", 16, 128, 32
+    codes = rng.integers(0, 16, (N, K))
+    sw = rng.uniform(0.01, 0.02, (N, K // G)).astype(np.float32)
+    wbuf = O.pack_file(fmt, codes, sw)
+    levels = codes - 8
+    deq = np.repeat(sw.astype(np.float64), G, axis=1) * levels          # [N, K]
+    # RMSNorm with constant x = c and gamma = 1: a = c / sqrt(c^2 + eps), q = 127 * sign(c)
+    for c in (1.5, -0.375, 3.0):
+        x = torch.full((1, K), c).to(torch.bfloat16)
+        r = O.forward(fmt, "rmsnorm", N, K, G, wbuf, x=bits_of(x), gamma=np.ones(K, np.float32), eps=1e-6)
+        a = c / np.sqrt(c * c + 1e-6)
+        assert np.all(r["q"] == 127 * np.sign(c))
+        assert np.allclose(r["y64"][0], a * deq.sum(axis=1), rtol=1e-12), c
+        assert np.array_equal(r["acc"][0], 127 * int(np.sign(c)) * levels.reshape(N, K // G, G).sum(axis=2))
+    # SwiGLU with gate = 0 gives 0; with gate = 20, silu(20) = 20 / (1 + e^-20)
+    up = torch.randn(2, K, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+    r = O.forward(fmt, "swiglu", N, K, G, wbuf, gate=bits_of(torch.zeros(2, K, dtype=torch.bfloat16)), up=bits_of(up))
+    assert np.all(r["y"] == 0) and np.all(r["s"] == 0)
+    r = O.forward(fmt, "swiglu", N, K, G, wbuf, gate=bits_of(torch.full((2, K), 20.0, dtype=torch.bfloat16)), up=bits_of(up))
+    from scipy.special import expit
+    assert np.allclose(r["a"], 20.0 * expit(20.0) * up.double().numpy(), rtol=1e-14)
+
+
+def check_invariants(O, seed=6):
+    rng = np.random.default_rng(seed)
+    for fmt in ("w4a8", "w6a8"):
+        b = {"w4a8": 4, "w6a8": 6}[fmt]
+        N, K, G = 32, 256, 64
+        codes = rng.integers(0, 1 << b, (N, K))
+        sw = rng.uniform(0.01, 0.02, (N, K // G)).astype(np.float32)
+        x = torch.randn(8, K, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+        xb = bits_of(x)
+        base = O.forward(fmt, "none", N, K, G, O.pack_file(fmt, codes, sw), x=xb)
+        # zero-level codes give 0
+        z = O.forward(fmt, "none", N, K, G, O.pack_file(fmt, np.full((N, K), 1 << (b - 1)), sw), x=xb)
+        assert np.all(z["y"] == 0) and np.all(z["acc"] == 0)
+        # zero scales give 0
+        z = O.forward(fmt, "none", N, K, G, O.pack_file(fmt, codes, np.zeros_like(sw)), x=xb)
+        assert np.all(z["y"] == 0)
+        # doubling every scale doubles y exactly
+        d = O.forward(fmt, "none", N, K, G, O.pack_file(fmt, codes, 2 * sw), x=xb)
+        assert np.array_equal(d["y64"], 2 * base["y64"])
+        # permuting the groups of K together with x leaves y unchanged
+        perm = rng.permutation(K // G)
+        kperm = (perm[:, None] * G + np.arange(G)[None, :]).reshape(-1)
+        p = O.forward(fmt, "none", N, K, G, O.pack_file(fmt, codes[:, kperm], sw[:, perm]), x=xb[:, kperm])
+        assert np.allclose(p["y64"], base["y64"], rtol=1e-13, atol=1e-13 * np.abs(base["y64"]).max())
+        # rows are independent: row m of the 8-row call equals the 1-row call
+        for m in (0, 5, 7):
+            one = O.forward(fmt, "none", N, K, G, O.pack_file(fmt, codes, sw), x=xb[m:m + 1])
+            assert np.array_equal(one["y"][0], base["y"][m])
+        # group sums agree with an int64 einsum (library route)
+        acc = np.einsum("mgk,ngk->mng", base["q"].reshape(8, K // G, G), (codes - (1 << (b - 1))).reshape(N, K // G, G))
+        assert np.array_equal(acc, base["acc"])
+
+
+def check_stream_positions(O):
+    g = read_golden("stream_positions.txt")
+    N, K, G = 16, 32, 32
+    rows = [[int(key)] + [int(v) for v in rest] for key in ("0", "9", "3", "15") for rest in g[key]]
+    for fmt in ("w4a8", "w6a8"):
+        size = O.file_bytes(fmt, N, K, G)
+        for n, k, nb, ns, hb, hs in rows:
+            buf = np.zeros(size, dtype=np.uint8)
+            buf[nb] = 0x5 << ns
+            if fmt == "w6a8":
+                buf[hb] = 0x2 << hs
+            codes, _ = O.unpack_stream(fmt, N, K, G, buf)
+            want = np.zeros((N, K), dtype=np.int64)
+            want[n, k] = 5 + (32 if fmt == "w6a8" else 0)
+            assert np.array_equal(codes, want), (fmt, n, k, np.argwhere(codes))
+        # scale order within the scale block
+        buf = np.zeros(size, dtype=np.uint8)
+        buf[:64] = np.arange(16, dtype="<f4").view(np.uint8)
+        _, sw = O.unpack_stream(fmt, N, K, G, buf)
+        for slot, row in enumerate(int(v) for v in g["scale_rows"][0]):
+            assert sw[row, 0] == slot, (fmt, row, sw[:, 0])
+
+
+def check_stream_bijection(O):
+    """Every code is read from its own field of the stream, and no two codes share one.
+
+    Each byte p of the buffer is labelled with its index, one 4-bit (or 2-bit)
+    digit at a time, by writing the digit into every field of the byte; the
+    unpacked code at (n, k) then reports the digit of the byte it came from.
+    Ragged tile (N % 128 != 0), several units, and G > 128 are covered."""
+    for fmt, N, K, G in (("w4a8", 144, 160, 32), ("w6a8", 144, 160, 32), ("w4a8", 32, 256, 256), ("w6a8", 16, 512, 256)):
+        size = O.file_bytes(fmt, N, K, G)
+        assert size < (1 << 16)
+        p = np.arange(size)
+        src = np.zeros((N, K), dtype=np.int64)
+        for j in range(4):
+            d = ((p >> (4 * j)) & 0xF).astype(np.uint8)
+            codes, _ = O.unpack_stream(fmt, N, K, G, d | (d << 4))
+            src |= (codes & 0xF) << (4 * j)
+        half, _ = O.unpack_stream(fmt, N, K, G, np.full(size, 0x10, dtype=np.uint8))
+        key = src * 2 + ((half & 0xF) >> 0)      # 0 = low nibble, 1 = high nibble
+        assert np.unique(key).size == N * K, fmt
+        if fmt == "w6a8":
+            hsrc = np.zeros((N, K), dtype=np.int64)
+            for j in range(8):
+                d = ((p >> (2 * j)) & 0x3).astype(np.uint8)
+                codes, _ = O.unpack_stream(fmt, N, K, G, d * np.uint8(0x55))
+                hsrc |= (codes >> 4) << (2 * j)
+            slot, _ = O.unpack_stream(fmt, N, K, G, np.full(size, 0b11100100, dtype=np.uint8))
+            hkey = hsrc * 4 + (slot >> 4)
+            assert np.unique(hkey).size == N * K, fmt
+            assert not np.intersect1d(src, hsrc).size, "2-bit plane shares bytes with the 4-bit plane"
