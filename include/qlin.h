@@ -1,0 +1,214 @@
+/*
+ * qlin -- skinny W4A8 / W6A8 quantized linear for GB300 (sm_103a).
+ *
+ *   y[M, N] = s_m * sum_g sw[n, g] * sum_{k in group g} q[m, k] * level[n, k]
+ *
+ * for M = 1..8 rows (one decoded token plus up to seven multi-token-prediction
+ * drafts), with level = code - 2^(b-1) from b = 4 or 6 bit weight codes, fp32
+ * group scales sw, and q = per-row int8 quantisation of the activation, which
+ * is x itself, RMSNorm(x) or silu(gate) * up.
+ *
+ * Sources (page title, section):
+ *  [LIN]  "Doubling the LLM token rate in ComfyUI", section "Optimising the
+ *         linear kernel": skinny GEMV for M = 1 and thin MTP verification M;
+ *         weights and per-group scales interleaved in the order the kernel
+ *         reads them, rearranged once per model load in place in VRAM; the M
+ *         rows mapped onto the 8-wide side of a tensor-core MMA so that up to
+ *         eight rows cost about what one row costs; the activation
+ *         quantisation absorbs the RMSNorm or SwiGLU in front of it.
+ *  [BOT]  same page, section "What is the bottleneck?": every token reads
+ *         every weight once, so decode speed is VRAM read speed.
+ *  [MTP]  same page, section "Adaptive-tree MTP": verification carries at
+ *         most eight rows (one committed token plus seven drafts).
+ *  [FMT]  "Comfy Quantization Formats", section "Weight formats": N output
+ *         width, K input width, G group size, FP32 scales.
+ *  [OPT]  same page, section "Format options": asym_w4a8_int8 (uniform levels
+ *         without a codebook) and w6a8_int8; symmetric weights; grouped W4A8
+ *         needs K % 16 == 0, K % G == 0, G >= 4 and (16 % G == 0 or
+ *         G % 16 == 0); W6A8 needs K % 32 == 0 and G % 16 == 0; backends may
+ *         restrict shapes further.
+ *  [ACT]  same page, section "Activations and smoothing": integer formats take
+ *         float activations and quantise them inside the kernel; no stored
+ *         input scale.
+ *
+ * Conventions for every entry point:
+ *  - All buffer pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or synchronises (except qlin_read_device_status).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) on the current device.
+ *  - Argument and shape errors are returned before anything is enqueued.
+ *    Launch failures return QLIN_ERR_CUDA.  A device-side bounded wait that
+ *    expires writes QLIN_ERR_DEVICE_TIMEOUT into the workspace status word,
+ *    read back by qlin_read_device_status; the kernel returns instead of
+ *    hanging.
+ *  - fmt is QLIN_W4A8 or QLIN_W6A8; b = 4 or 6 bits per code.
+ *  - Backend limits beyond [OPT] (QLIN_ERR_UNSUPPORTED): G in {32, 64, 128,
+ *    256} (so K % 32 == 0), N % 16 == 0, K <= 98304, M <= 8.
+ */
+#ifndef QLIN_H_
+#define QLIN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QLIN_OK = 0,
+  QLIN_ERR_INVALID_ARG = 1,    /* bad pointer, alignment, size, or a shape [OPT] forbids */
+  QLIN_ERR_UNSUPPORTED = 2,    /* legal per [OPT] but outside this backend's limits */
+  QLIN_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+  QLIN_ERR_DEVICE_TIMEOUT = 4, /* a device-side bounded wait expired (status word) */
+  QLIN_ERR_WORKSPACE = 5       /* workspace smaller than the size query returned */
+} qlin_status;
+
+typedef enum { QLIN_W4A8 = 0, QLIN_W6A8 = 1 } qlin_format;
+
+typedef enum {
+  QLIN_PROLOGUE_NONE = 0,    /* a = x */
+  QLIN_PROLOGUE_RMSNORM = 1, /* a = x * gamma / sqrt(mean(x^2) + eps) */
+  QLIN_PROLOGUE_SWIGLU = 2   /* a = gate / (1 + exp(-gate)) * up */
+} qlin_prologue;
+
+/* qlin_forward flags. */
+#define QLIN_FLAG_PDL 1u /* Launch with programmatic dependent launch: the GEMV may start
+                            streaming `packed` while earlier kernels in `stream` still run.
+                            The caller asserts that `packed` was not written by any kernel
+                            still in flight in `stream` (true for model weights repacked
+                            at load time).  Activations, gamma, y and the workspace are
+                            still touched only after earlier kernels complete. */
+
+/* Library version string. */
+const char* qlin_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* qlin_status_string(qlin_status s);
+
+/* Validate a weight shape against [OPT] and the backend limits.  Host only.
+ * Returns QLIN_OK, QLIN_ERR_INVALID_ARG or QLIN_ERR_UNSUPPORTED. */
+qlin_status qlin_check_shape(int fmt, int64_t N, int64_t K, int64_t G);
+
+/* Bytes of one quantized weight, in either layout: N*K*b/8 code bytes plus
+ * N*(K/G)*4 scale bytes [FMT].  0 when qlin_check_shape fails. */
+size_t qlin_packed_bytes(int fmt, int64_t N, int64_t K, int64_t G);
+
+/*
+ * In-place repack [LIN]: rewrites `buf` from the checkpoint layout into the
+ * kernel-order stream that qlin_forward reads.  Same size in and out
+ * (qlin_packed_bytes).  One call per weight, once per load; calling it twice
+ * does not give the same bytes as calling it once.
+ *
+ * Checkpoint layout (input): codes, then scales.
+ *   4-bit: uint8 [N, K/2], low nibble = even k.  6-bit: uint8 [N, 3K/4], each 3
+ *   bytes a little-endian 24-bit word holding 4 codes, code i at bits 6i..6i+5.
+ *   Scales: fp32 [N, K/G] row-major, little-endian, right after the codes.
+ * Stream layout (output), KB = max(128, G):
+ *   tiles of 128 output rows (the last may hold fewer, a multiple of 16), in
+ *   order; inside a tile, units of KB input columns (the last may be
+ *   narrower), in order; a unit of R rows and W columns is
+ *     scale block  R*(W/G) fp32: for each group of the unit, for each 16-row
+ *                  slab, for p = 0..7: sw[row p], sw[row p + 8];
+ *     code block   for each slab, for each pair of 16-wide k-steps:
+ *                  4-bit plane: 32 lanes x {word for step A, word for step B};
+ *                  6-bit codes only, then the 2-bit plane: 32 lanes x 1 word.
+ *   A lane (g, t) = (lane / 4, lane % 4) holds the A operand of a 16x16 bf16
+ *   tensor-core tile: register i in 0..3 holds (row g, k 2t..2t+1),
+ *   (row g+8, k 2t..2t+1), (row g, k 2t+8..2t+9), (row g+8, k 2t+8..2t+9).  In
+ *   a 4-bit plane word, register i's two elements sit at bits 4i..4i+3 and
+ *   16+4i..16+4i+3 (the low 4 bits of the code).  In the 2-bit plane word the
+ *   top 2 bits of step A register i sit at bits 2i and 16+2i, those of step B
+ *   at bits 8+2i and 24+2i.  Codes are stored unsigned (not offset).
+ *
+ * buf: device, 16-byte aligned, qlin_packed_bytes(fmt, N, K, G) bytes.
+ * ws : device scratch, 256-byte aligned, at least *min_bytes from
+ *      qlin_repack_workspace_bytes; larger means fewer, bigger copy waves.
+ *      Strictly zero extra memory is not possible because codes and scales sit
+ *      in separate regions of the input; the scratch holds all scales plus one
+ *      wave of 128-row code tiles.
+ */
+qlin_status qlin_repack_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t G,
+                                        size_t* min_bytes, size_t* recommended_bytes);
+qlin_status qlin_repack(int fmt, int64_t N, int64_t K, int64_t G, void* buf,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Forward workspace [LIN]: holds the status word, the per-row scales, the
+ * quantised activation operand, the split-K tile counters and the split-K
+ * partial sums.  Its size depends on the current device's SM count.  Zero it
+ * once with qlin_workspace_init before its first use (that clears the status
+ * word; each call resets its own split-K counters).  One workspace may serve
+ * every layer of a model, of any shape (size it for the largest), as long as
+ * the calls using it are ordered on one stream.
+ */
+qlin_status qlin_forward_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t G, size_t* bytes);
+qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * y = packed-weight x quantised activation [LIN], [ACT], [MTP].
+ *   fmt, prologue : qlin_format, qlin_prologue.
+ *   M             : rows, 1..8 (M = 0 or N = 0 enqueues nothing).
+ *   packed        : device, repacked stream (qlin_repack), 16-byte aligned.
+ *   x             : bf16 [M, K] row-major, 16-byte aligned (NONE, RMSNORM).
+ *   gate, up      : bf16 [M, K] row-major, 16-byte aligned (SWIGLU).
+ *   gamma         : fp32 [K], 16-byte aligned (RMSNORM); eps >= 0 (RMSNORM).
+ *   y             : fp32 [M, N] row-major, 4-byte aligned; fully overwritten.
+ *   ws, ws_bytes  : forward workspace (see above), 256-byte aligned.
+ *   flags         : 0 or QLIN_FLAG_PDL.
+ * Numerics: the prologue and the scale s_m = amax/127 are computed in fp32,
+ * q = clamp(round-half-even(a / s_m), -127, 127) (s_m = 0, q = 0 for an
+ * all-zero row); group sums are exact integers; y is accumulated in fp32 in a
+ * fixed order that depends on (N, K, G) and the device, never on M or on the
+ * other rows, so row m of an 8-row call equals the same row run alone.
+ * Two kernels are enqueued: the fused prologue + quantisation, then the GEMV
+ * with its in-launch split-K reduction.
+ */
+qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
+                         const void* packed, const void* x, const void* gate, const void* up,
+                         const float* gamma, float eps, float* y,
+                         void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/* Launch shape of qlin_forward's GEMV on the current device: CTAs, stream
+ * units (128 rows x KB columns) and bytes of `packed` read per call. */
+qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G,
+                                     int64_t* ctas, int64_t* units, int64_t* stream_bytes);
+
+/* Synchronises `stream`, then returns the workspace status word (QLIN_OK when
+ * no device-side wait has expired since qlin_workspace_init).  For tests. */
+qlin_status qlin_read_device_status(const void* ws, void* stream);
+
+/*
+ * Test exports: the same kernels, with extra outputs.
+ * qlin_debug_quantize_act runs the prologue kernel alone and unpacks its
+ * operand: q int8 [M, K] row-major and s fp32 [M] (device pointers).  Needs a
+ * forward workspace for (fmt, N = 16, K, G) at least.
+ * qlin_debug_group_acc runs qlin_forward and also writes the exact group sums
+ * acc int32 [M, N, K/G] (device); y may be NULL.
+ */
+qlin_status qlin_debug_quantize_act(int fmt, int prologue, int M, int64_t K, int64_t G,
+                                    const void* x, const void* gate, const void* up,
+                                    const float* gamma, float eps, int8_t* q, float* s,
+                                    void* ws, size_t ws_bytes, void* stream);
+qlin_status qlin_debug_group_acc(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
+                                 const void* packed, const void* x, const void* gate, const void* up,
+                                 const float* gamma, float eps, float* y, int32_t* acc,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Test export for failure detection: qlin_forward, except that the GEMV never
+ * issues the copy of stream unit `unit` (0 <= unit < units).  The consumers'
+ * bounded wait on that unit expires after about a second; the kernel writes
+ * QLIN_ERR_DEVICE_TIMEOUT into the workspace status word, waits (bounded) for
+ * the copies it did issue, and returns, leaving the context usable and the
+ * workspace counters at zero.  y is unspecified afterwards.  Nothing faults.
+ */
+qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
+                                     const void* packed, const void* x, const void* gate, const void* up,
+                                     const float* gamma, float eps, float* y, void* ws, size_t ws_bytes,
+                                     int64_t unit, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QLIN_H_ */

@@ -93,15 +93,19 @@ def file_bytes(fmt: str, N: int, K: int, G: int) -> int:
 # 1. checkpoint layout
 # ----------------------------------------------------------------------------
 
-def unpack_file(fmt: str, N: int, K: int, G: int, buf) -> tuple[np.ndarray, np.ndarray]:
+def unpack_file(fmt: str, N: int, K: int, G: int, buf, rows=None) -> tuple[np.ndarray, np.ndarray]:
     """Split a checkpoint-layout buffer into codes int64 [N, K] and fp32 scales [N, K/G].
 
+    ``rows`` (optional) selects output rows n to unpack, for sampled checks.
     "Comfy Quantization Formats", section "Weight formats" (N, K, G, FP32
     scales); bit order per the reading in the module docstring."""
     buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
     ncb = file_code_bytes(fmt, N, K)
     assert buf.size >= file_bytes(fmt, N, K, G)
-    cb = buf[:ncb].reshape(N, K * BITS[fmt] // 8).astype(np.int64)
+    N_all = N
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    cb = buf[:ncb].reshape(N, K * BITS[fmt] // 8)[rows].astype(np.int64)
+    N = rows.size
     codes = np.empty((N, K), dtype=np.int64)
     if BITS[fmt] == 4:
         codes[:, 0::2] = cb & 0xF
@@ -111,8 +115,8 @@ def unpack_file(fmt: str, N: int, K: int, G: int, buf) -> tuple[np.ndarray, np.n
         word = t[..., 0] | (t[..., 1] << 8) | (t[..., 2] << 16)
         for i in range(4):
             codes[:, i::4] = (word >> (6 * i)) & 0x3F
-    sw = np.frombuffer(buf[ncb:ncb + file_scale_bytes(N, K, G)].tobytes(), dtype="<f4")
-    return codes, sw.reshape(N, K // G).astype(np.float32)
+    sw = np.frombuffer(buf[ncb:ncb + file_scale_bytes(N_all, K, G)].tobytes(), dtype="<f4")
+    return codes, sw.reshape(N_all, K // G)[rows].astype(np.float32)
 
 
 def pack_file(fmt: str, codes, sw) -> np.ndarray:
@@ -247,11 +251,10 @@ def forward(fmt: str, kind: str, N: int, K: int, G: int, buf, x=None, gate=None,
     """
     if stream:
         codes, sw = unpack_stream(fmt, N, K, G, buf)
+        if cols is not None:
+            codes, sw = codes[cols], sw[cols]
     else:
-        codes, sw = unpack_file(fmt, N, K, G, buf)
-    if cols is not None:
-        cols = np.asarray(cols, dtype=np.int64)
-        codes, sw = codes[cols], sw[cols]
+        codes, sw = unpack_file(fmt, N, K, G, buf, rows=cols)
     a = prologue(kind, x=x, gate=gate, up=up, gamma=gamma, eps=eps)
     q, s, v = quantize_rows(a, fp32=(kind == "none"))
     acc = group_acc(q, codes, fmt, G)

@@ -26,7 +26,7 @@ MUTANTS = {
     "swiglu_operands_swapped": ("gv / (1.0 + np.exp(-gv)) * uv", "uv / (1.0 + np.exp(-uv)) * gv"),
     "rmsnorm_mean_over_k_minus_1": ("(xv * xv).sum(axis=1) / K", "(xv * xv).sum(axis=1) / (K - 1)"),
     "group_scale_shifted": ("sw.astype(np.float64)[None, :, :]", "np.roll(sw, 1, axis=1).astype(np.float64)[None, :, :]"),
-    "scale_matrix_transposed": ("sw.reshape(N, K // G).astype(np.float32)", "sw.reshape(K // G, N).T.astype(np.float32)"),
+    "scale_matrix_transposed": ("sw.reshape(N_all, K // G)[rows]", "sw.reshape(K // G, N_all).T[rows]"),
     "row_scale_dropped": ("y64 = s[:, None] * (", "y64 = 1.0 * ("),
     "acc_sign_flipped": ("L = np.asarray(codes, dtype=np.int64) - code_offset(fmt)", "L = code_offset(fmt) - np.asarray(codes, dtype=np.int64)"),
     "stream_hi_bits_moved": ("(8 * step + 16 * elem + 2 * reg)", "(8 * step + 16 * elem + 2 * (3 - reg))"),

@@ -1,0 +1,104 @@
+// Geometry of the kernel-order weight stream and of the forward workspace.
+// Shared by the host planner and the kernels of this library (one build).
+//
+// Stream: tiles of TILE_N = 128 output rows; in a tile, units of KB = max(128, G)
+// input columns; a unit is [scale block][code block] (layout documented with
+// qlin_repack in qlin.h).  The rearrangement into the order the kernel reads
+// follows "Doubling the LLM token rate in ComfyUI", section "Optimising the
+// linear kernel" (weights and group scales interleaved so each thread block
+// streams one contiguous segment).
+#pragma once
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define QL_HD __host__ __device__ __forceinline__
+#else
+#define QL_HD inline
+#endif
+
+namespace qlin {
+
+constexpr int TILE_N = 128;        // output rows per tile
+constexpr int SLAB = 16;           // rows of one tensor-core A tile
+constexpr int KSTEP = 16;          // k per bf16 MMA
+constexpr int PAIR_K = 32;         // two k-steps share one plane word pair
+constexpr int MAX_M = 8;           // rows of the activation (N side of the MMA)
+constexpr int CONSUMER_WARPS = 4;  // each owns two slabs (32 rows) of a tile
+constexpr int GEMV_THREADS = (CONSUMER_WARPS + 1) * 32;
+constexpr int MAX_STAGES = 16;
+constexpr int WS_HEADER = 256;     // status word + row scales
+constexpr int WS_SCALE_OFF = 64;   // fp32 s[8] inside the header
+constexpr int PARTIAL_FLOATS = CONSUMER_WARPS * 32 * 8;  // one tile's split-K partial
+constexpr int PROLOGUE_THREADS = 256;
+constexpr int64_t MAX_K = 98304;
+
+QL_HD int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+QL_HD int64_t kb_of(int64_t G) { return G > 128 ? G : 128; }
+QL_HD int bits_of(int fmt) { return fmt == 1 ? 6 : 4; }
+QL_HD int code_offset(int bits) { return 1 << (bits - 1); }
+// bytes of one 16-row x 32-k piece of the code block
+QL_HD int pair_bytes(int bits) { return bits == 6 ? 384 : 256; }
+
+// bytes of a unit of R rows and W columns
+QL_HD int64_t unit_bytes(int bits, int64_t R, int64_t W, int64_t G) {
+  return R * (W / G) * 4 + R * W * bits / 8;
+}
+// bytes of the activation operand block for W columns: bf16 fragments, then
+// one float pair block (8 rows) of -(128 + offset) * sum(q) per group
+QL_HD int64_t bblock_bytes(int64_t W, int64_t G) { return W * 16 + (W / G) * 32; }
+
+struct Geo {
+  int bits;
+  int64_t N, K, G, KB;
+  int64_t T;        // tiles
+  int64_t J;        // units per tile
+  int64_t U;        // units
+  int64_t tile_full;   // bytes of a 128-row tile
+  int64_t bbf;         // bytes of a full activation block (stride)
+  int64_t unit_full;   // bytes of a full 128-row unit
+};
+
+QL_HD Geo make_geo(int fmt, int64_t N, int64_t K, int64_t G) {
+  Geo g;
+  g.bits = bits_of(fmt);
+  g.N = N; g.K = K; g.G = G;
+  g.KB = kb_of(G);
+  g.T = (N + TILE_N - 1) / TILE_N;
+  g.J = (K + g.KB - 1) / g.KB;
+  g.U = g.T * g.J;
+  g.tile_full = unit_bytes(g.bits, TILE_N, K, G);
+  g.bbf = bblock_bytes(g.KB, G);
+  g.unit_full = unit_bytes(g.bits, TILE_N, g.KB, G);
+  return g;
+}
+QL_HD int64_t tile_rows(const Geo& g, int64_t t) {
+  int64_t r = g.N - t * TILE_N;
+  return r < TILE_N ? r : TILE_N;
+}
+QL_HD int64_t unit_cols(const Geo& g, int64_t j) {
+  int64_t w = g.K - j * g.KB;
+  return w < g.KB ? w : g.KB;
+}
+QL_HD int64_t unit_offset(const Geo& g, int64_t t, int64_t j) {
+  return t * g.tile_full + j * unit_bytes(g.bits, tile_rows(g, t), g.KB, g.G);
+}
+
+// Forward workspace layout: [header][activation blocks][tile counters][partials]
+struct WsLayout {
+  int64_t b_off, cnt_off, part_off, total;
+};
+QL_HD WsLayout make_ws(const Geo& g, int64_t max_ctas) {
+  WsLayout w;
+  w.b_off = WS_HEADER;
+  w.cnt_off = w.b_off + round_up(g.J * g.bbf, 256);
+  w.part_off = w.cnt_off + round_up(g.T * 4, 256);
+  w.total = w.part_off + max_ctas * 2 * PARTIAL_FLOATS * 4;
+  return w;
+}
+
+// Split of U units over P CTAs: CTA p owns [p*U/P, (p+1)*U/P).
+QL_HD int64_t split_begin(int64_t p, int64_t U, int64_t P) { return p * U / P; }
+// CTA owning unit x
+QL_HD int64_t split_owner(int64_t x, int64_t U, int64_t P) { return ((x + 1) * P - 1) / U; }
+
+}  // namespace qlin

@@ -1,0 +1,221 @@
+"""Thin Python binding of libqlin (ctypes).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  There is no fallback:
+if the library is missing, every call raises.
+
+Names follow the C ABI in ``include/qlin.h`` without the ``qlin_`` prefix.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+FORMATS = {"w4a8": 0, "w6a8": 1}
+PROLOGUES = {"none": 0, "rmsnorm": 1, "swiglu": 2}
+FLAG_PDL = 1
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_WORKSPACE = range(6)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QlinError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libqlin.so from the package's build folder (no implicit build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libqlin.so is not built ({path}); run __graft_entry__.build() "
+                                   "or python -m w6a8_quantized_linear_gb300.build")
+            L = ctypes.CDLL(path)
+            i64, sz, vp, i32 = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
+            st = ctypes.c_int
+            sig = {
+                "qlin_version": (ctypes.c_char_p, []),
+                "qlin_status_string": (ctypes.c_char_p, [st]),
+                "qlin_check_shape": (st, [i32, i64, i64, i64]),
+                "qlin_packed_bytes": (sz, [i32, i64, i64, i64]),
+                "qlin_repack_workspace_bytes": (st, [i32, i64, i64, i64, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+                "qlin_repack": (st, [i32, i64, i64, i64, vp, vp, sz, vp]),
+                "qlin_forward_workspace_bytes": (st, [i32, i64, i64, i64, ctypes.POINTER(sz)]),
+                "qlin_workspace_init": (st, [vp, sz, vp]),
+                "qlin_forward": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz,
+                                      ctypes.c_uint, vp]),
+                "qlin_forward_launch_info": (st, [i32, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                                  ctypes.POINTER(i64)]),
+                "qlin_read_device_status": (st, [vp, vp]),
+                "qlin_debug_quantize_act": (st, [i32, i32, i32, i64, i64, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp,
+                                                 sz, vp]),
+                "qlin_debug_group_acc": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                              vp, sz, vp]),
+                "qlin_debug_forward_fault": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp,
+                                                  vp, sz, i64, vp]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().qlin_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().qlin_version().decode()
+
+
+def _fmt(f) -> int:
+    return FORMATS[f] if isinstance(f, str) else int(f)
+
+
+def _pro(p) -> int:
+    return PROLOGUES[p] if isinstance(p, str) else int(p)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise QlinError(status, where)
+
+
+def check_shape(fmt, N: int, K: int, G: int) -> int:
+    return lib().qlin_check_shape(_fmt(fmt), N, K, G)
+
+
+def packed_bytes(fmt, N: int, K: int, G: int) -> int:
+    return lib().qlin_packed_bytes(_fmt(fmt), N, K, G)
+
+
+def repack_workspace_bytes(fmt, N: int, K: int, G: int) -> tuple[int, int]:
+    lo, rec = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().qlin_repack_workspace_bytes(_fmt(fmt), N, K, G, ctypes.byref(lo), ctypes.byref(rec)),
+           "repack_workspace_bytes")
+    return lo.value, rec.value
+
+
+def repack(buf: torch.Tensor, fmt, N: int, K: int, G: int, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Rewrite ``buf`` (uint8, checkpoint layout, on the GPU) into the kernel-order stream, in place."""
+    if ws is None:
+        _, rec = repack_workspace_bytes(fmt, N, K, G)
+        ws = torch.empty(rec, dtype=torch.uint8, device=buf.device)
+    _check(lib().qlin_repack(_fmt(fmt), N, K, G, _ptr(buf), _ptr(ws), ws.numel(), _stream(stream)), "repack")
+    return buf
+
+
+def forward_workspace_bytes(fmt, N: int, K: int, G: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().qlin_forward_workspace_bytes(_fmt(fmt), N, K, G, ctypes.byref(n)), "forward_workspace_bytes")
+    return n.value
+
+
+def workspace_init(ws: torch.Tensor, stream=None) -> None:
+    _check(lib().qlin_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "workspace_init")
+
+
+def new_workspace(nbytes: int, device="cuda", stream=None) -> torch.Tensor:
+    """A zeroed forward workspace of ``nbytes`` (allocated by torch, zeroed by the library)."""
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    workspace_init(ws, stream)
+    return ws
+
+
+def forward(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, x=None, gate=None, up=None, gamma=None,
+            eps: float = 1e-6, y: torch.Tensor | None = None, ws: torch.Tensor | None = None, flags: int = 0,
+            stream=None) -> torch.Tensor:
+    """y[M, N] (fp32) = repacked weight x int8-quantised prologue(activation)."""
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.float32, device=packed.device)
+    if ws is None:
+        ws = new_workspace(forward_workspace_bytes(fmt, N, K, G), packed.device, stream)
+    _check(lib().qlin_forward(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate), _ptr(up),
+                              _ptr(gamma), float(eps), _ptr(y), _ptr(ws), ws.numel(), flags, _stream(stream)),
+           "forward")
+    return y
+
+
+def launch_info(fmt, N: int, K: int, G: int) -> dict:
+    c, u, b = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().qlin_forward_launch_info(_fmt(fmt), N, K, G, ctypes.byref(c), ctypes.byref(u), ctypes.byref(b)),
+           "launch_info")
+    return {"ctas": c.value, "units": u.value, "stream_bytes": b.value}
+
+
+def read_device_status(ws: torch.Tensor, stream=None) -> int:
+    return lib().qlin_read_device_status(_ptr(ws), _stream(stream))
+
+
+def debug_quantize_act(fmt, prologue, K: int, G: int, x=None, gate=None, up=None, gamma=None, eps: float = 1e-6,
+                       ws: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    dev = act.device
+    q = torch.empty(M, K, dtype=torch.int8, device=dev)
+    s = torch.empty(M, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = new_workspace(forward_workspace_bytes(fmt, 16, K, G), dev, stream)
+    _check(lib().qlin_debug_quantize_act(_fmt(fmt), _pro(prologue), M, K, G, _ptr(x), _ptr(gate), _ptr(up),
+                                         _ptr(gamma), float(eps), _ptr(q), _ptr(s), _ptr(ws), ws.numel(),
+                                         _stream(stream)), "debug_quantize_act")
+    return q, s
+
+
+def debug_group_acc(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, x=None, gate=None, up=None,
+                    gamma=None, eps: float = 1e-6, ws: torch.Tensor | None = None,
+                    stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    y = torch.empty(M, N, dtype=torch.float32, device=packed.device)
+    acc = torch.empty(M, N, K // G, dtype=torch.int32, device=packed.device)
+    if ws is None:
+        ws = new_workspace(forward_workspace_bytes(fmt, N, K, G), packed.device, stream)
+    _check(lib().qlin_debug_group_acc(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate),
+                                      _ptr(up), _ptr(gamma), float(eps), _ptr(y), _ptr(acc), _ptr(ws), ws.numel(),
+                                      _stream(stream)), "debug_group_acc")
+    return y, acc
+
+
+def debug_forward_fault(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, unit: int, x=None, gate=None,
+                        up=None, gamma=None, eps: float = 1e-6, y=None, ws: torch.Tensor | None = None,
+                        stream=None) -> int:
+    """Enqueue a forward whose GEMV never issues the copy of ``unit``; returns the enqueue status."""
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.float32, device=packed.device)
+    return lib().qlin_debug_forward_fault(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate),
+                                          _ptr(up), _ptr(gamma), float(eps), _ptr(y), _ptr(ws), ws.numel(), unit,
+                                          _stream(stream))
