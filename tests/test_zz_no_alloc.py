@@ -1,0 +1,56 @@
+"""qlin_forward_noalloc: the forward for callers that cannot allocate device
+memory where they run a layer (their memory pool owns the device, or they
+must avoid cudaMalloc's implicit synchronisation).  The entry point uses a
+fixed device array inside the library as its workspace.
+
+Checked through the C ABI against qlin_forward (with a caller workspace) on
+two calls in a row, which share the library's array.  Collected last on
+purpose; it passes alone in a fresh process too.
+"""
+import pytest
+import torch
+
+from gpu_util import DEV, assert_y_close, built, device_case, gpu_forward
+from w6a8_quantized_linear_gb300 import inputs, qlin
+
+pytestmark = pytest.mark.gpu
+
+LIMIT = 4 << 20
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    built()
+    torch.cuda.set_device(DEV)
+
+
+def test_noalloc_matches_forward_two_calls_in_a_row():
+    cases = [inputs.make_case("w4a8", "rmsnorm", 8, 6144, 5120, 128, seed=31, device="cpu"),
+             inputs.make_case("w6a8", "swiglu", 3, 1040, 1056, 32, seed=32, device="cpu")]
+    devs = [device_case(c) for c in cases]
+    refs = [gpu_forward(c, d) for c, d in zip(cases, devs)]
+    outs = []
+    for c, d in zip(cases, devs):  # two calls in a row on the shared array
+        outs.append(qlin.forward_noalloc(c.fmt, c.kind, d["w"], c.N, c.K, c.G, x=d["x"], gate=d["gate"],
+                                         up=d["up"], gamma=d["gamma"], eps=c.eps))
+    torch.cuda.synchronize()
+    for c, r, o in zip(cases, refs, outs):
+        assert_y_close(o.cpu().numpy(), r.double().cpu().numpy(), f"noalloc {c.fmt} {c.kind}")
+    # and again, after the array holds the second call's contents
+    again = qlin.forward_noalloc(cases[0].fmt, cases[0].kind, devs[0]["w"], cases[0].N, cases[0].K, cases[0].G,
+                                 x=devs[0]["x"], gamma=devs[0]["gamma"], eps=cases[0].eps)
+    assert_y_close(again.cpu().numpy(), refs[0].double().cpu().numpy(), "noalloc repeat")
+
+
+def test_noalloc_rejects_shapes_beyond_its_array():
+    big = [(f, N, K, G) for f, N, K, G in (("w6a8", 16, 98304, 32), ("w4a8", 16, 98304, 32))
+           if qlin.forward_workspace_bytes(f, N, K, G) > LIMIT]
+    if not big:
+        pytest.skip("every supported shape fits the array on this device")
+    f, N, K, G = big[0]
+    w = torch.zeros(qlin.packed_bytes(f, N, K, G), dtype=torch.uint8, device=DEV)
+    x = torch.zeros(1, K, dtype=torch.bfloat16, device=DEV)
+    y = torch.empty(1, N, dtype=torch.float32, device=DEV)
+    st = qlin.lib().qlin_forward_noalloc(qlin.FORMATS[f], 0, 1, N, K, G, w.data_ptr(), x.data_ptr(), None, None,
+                                         None, 1e-6, y.data_ptr(), 0, torch.cuda.current_stream().cuda_stream)
+    assert st == qlin.ERR_WORKSPACE

@@ -275,6 +275,38 @@ qlin_status forward_impl(int fmt, int kind, int M, int64_t N, int64_t K, int64_t
   return launch(fn, dim3((unsigned)p.P, 1, 1), dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, s, args, 0, true);
 }
 
+// ---------------------------------------------------------------------------
+// Scratch for qlin_forward_noalloc: a fixed device array owned by the library.
+// Some callers cannot allocate device memory at the point where they run the
+// layer (a host that hands all memory to its own pool and forbids further
+// cudaMalloc, code that must not take cudaMalloc's implicit device-wide
+// synchronisation, or a deployment that fixes its memory footprint up
+// front).  They use this array instead of a caller-provided workspace.  Every
+// GPU that loads the library holds it until the process exits.
+constexpr size_t NOALLOC_SCRATCH_BYTES = 4u << 20;  // 4 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of the array on the current device, looked up once per
+// device (host code cannot use the array's name as a device address).
+qlin_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= 64) return QLIN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return QLIN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -450,6 +482,22 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
   if (unit < 0) return QLIN_ERR_INVALID_ARG;
   return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, y, nullptr, ws, ws_bytes, 0, stream,
                       false, unit);
+}
+
+qlin_status qlin_forward_noalloc(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
+                                 const void* packed, const void* x, const void* gate, const void* up,
+                                 const float* gamma, float eps, float* y, unsigned flags, void* stream) {
+  qlin_status st = check_shape_impl(fmt, N, K, G);
+  if (st != QLIN_OK) return st;
+  size_t need = 0;
+  st = qlin_forward_workspace_bytes(fmt, N, K, G, &need);
+  if (st != QLIN_OK) return st;
+  if (need > NOALLOC_SCRATCH_BYTES) return QLIN_ERR_WORKSPACE;
+  void* ws = nullptr;
+  st = noalloc_scratch(&ws);
+  if (st != QLIN_OK) return st;
+  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, y, nullptr, ws,
+                      NOALLOC_SCRATCH_BYTES, flags, stream, false);
 }
 
 }  // extern "C"

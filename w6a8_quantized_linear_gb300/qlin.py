@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
                                               vp, sz, vp]),
                 "qlin_debug_forward_fault": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp,
                                                   vp, sz, i64, vp]),
+                "qlin_forward_noalloc": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp,
+                                              ctypes.c_uint, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -164,6 +166,21 @@ def forward(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, x=None,
     _check(lib().qlin_forward(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate), _ptr(up),
                               _ptr(gamma), float(eps), _ptr(y), _ptr(ws), ws.numel(), flags, _stream(stream)),
            "forward")
+    return y
+
+
+def forward_noalloc(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, x=None, gate=None, up=None,
+                    gamma=None, eps: float = 1e-6, y: torch.Tensor | None = None, flags: int = 0,
+                    stream=None) -> torch.Tensor:
+    """``forward`` for callers that cannot allocate device memory: the library
+    uses its own fixed 4 MiB device array as the workspace (see qlin.h)."""
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.float32, device=packed.device)
+    _check(lib().qlin_forward_noalloc(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate),
+                                      _ptr(up), _ptr(gamma), float(eps), _ptr(y), flags, _stream(stream)),
+           "forward_noalloc")
     return y
 
 
