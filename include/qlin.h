@@ -43,7 +43,7 @@
  *    hanging.
  *  - fmt is QLIN_W4A8 or QLIN_W6A8; b = 4 or 6 bits per code.
  *  - Backend limits beyond [OPT] (QLIN_ERR_UNSUPPORTED): G in {32, 64, 128,
- *    256} (so K % 32 == 0), N % 16 == 0, K <= 98304, M <= 8.
+ *    256} (so K % 32 == 0), N % 16 == 0, K <= 65536, M <= 8.
  */
 #ifndef QLIN_H_
 #define QLIN_H_
@@ -134,13 +134,11 @@ qlin_status qlin_repack(int fmt, int64_t N, int64_t K, int64_t G, void* buf,
                         void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Forward workspace [LIN]: holds the status word, the per-row scales, the
- * quantised activation operand, the split-K tile counters and the split-K
- * partial sums.  Its size depends on the current device's SM count.  Zero it
- * once with qlin_workspace_init before its first use (that clears the status
- * word; each call resets its own split-K counters).  One workspace may serve
- * every layer of a model, of any shape (size it for the largest), as long as
- * the calls using it are ordered on one stream.
+ * Forward workspace: one status word (plus reserved bytes) that a device-side
+ * wait which expires sets to QLIN_ERR_DEVICE_TIMEOUT.  Zero it once with
+ * qlin_workspace_init; one workspace may serve every call of a model.  The
+ * forward keeps everything else (the quantised activations, the split-K
+ * partial sums) in on-chip shared memory.
  */
 qlin_status qlin_forward_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t G, size_t* bytes);
 qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream);
@@ -158,11 +156,14 @@ qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream);
  *   flags         : 0 or QLIN_FLAG_PDL.
  * Numerics: the prologue and the scale s_m = amax/127 are computed in fp32,
  * q = clamp(round-half-even(a / s_m), -127, 127) (s_m = 0, q = 0 for an
- * all-zero row); group sums are exact integers; y is accumulated in fp32 in a
- * fixed order that depends on (N, K, G) and the device, never on M or on the
- * other rows, so row m of an 8-row call equals the same row run alone.
- * Two kernels are enqueued: the fused prologue + quantisation, then the GEMV
- * with its in-launch split-K reduction.
+ * all-zero row; with no prologue a / s_m is the IEEE fp32 quotient, with a
+ * prologue a * (127 / amax)); group sums are exact integers; y is accumulated
+ * in fp32 in a fixed order that depends on (N, K, G) and the device, never on
+ * M or on the other rows, so row m of an 8-row call equals the same row run
+ * alone.  One kernel is enqueued: a cluster of CTAs per 256 output rows
+ * splits K, computes the prologue and the row statistics in shared memory,
+ * streams the weights through the tensor cores and reduces its split-K
+ * partial sums through distributed shared memory.
  */
 qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
                          const void* packed, const void* x, const void* gate, const void* up,
@@ -179,29 +180,24 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G,
 qlin_status qlin_read_device_status(const void* ws, void* stream);
 
 /*
- * Test exports: the same kernels, with extra outputs.
- * qlin_debug_quantize_act runs the prologue kernel alone and unpacks its
- * operand: q int8 [M, K] row-major and s fp32 [M] (device pointers).  Needs a
- * forward workspace for (fmt, N = 16, K, G) at least.
- * qlin_debug_group_acc runs qlin_forward and also writes the exact group sums
- * acc int32 [M, N, K/G] (device); y may be NULL.
+ * Test export: qlin_forward with extra outputs (device pointers, each may be
+ * NULL): y fp32 [M, N]; acc int32 [M, N, K/G], the exact per-group integer
+ * sums sum_k q[m,k] * level[n,k]; q int8 [M, K], the activation codes; s fp32
+ * [M], the row scales.
  */
-qlin_status qlin_debug_quantize_act(int fmt, int prologue, int M, int64_t K, int64_t G,
-                                    const void* x, const void* gate, const void* up,
-                                    const float* gamma, float eps, int8_t* q, float* s,
-                                    void* ws, size_t ws_bytes, void* stream);
-qlin_status qlin_debug_group_acc(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
-                                 const void* packed, const void* x, const void* gate, const void* up,
-                                 const float* gamma, float eps, float* y, int32_t* acc,
-                                 void* ws, size_t ws_bytes, void* stream);
+qlin_status qlin_debug_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
+                               const void* packed, const void* x, const void* gate, const void* up,
+                               const float* gamma, float eps, float* y, int32_t* acc, int8_t* q, float* s,
+                               void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Test export for failure detection: qlin_forward, except that the GEMV never
- * issues the copy of stream unit `unit` (0 <= unit < units).  The consumers'
- * bounded wait on that unit expires after about a second; the kernel writes
+ * Test export for failure detection: qlin_forward, except that the first CTA
+ * of the launch never issues the weight copy of its local unit `unit` (0 is
+ * its first unit and always exists).  Its consumers' bounded wait on that
+ * unit expires after about a second; the kernel writes
  * QLIN_ERR_DEVICE_TIMEOUT into the workspace status word, waits (bounded) for
- * the copies it did issue, and returns, leaving the context usable and the
- * workspace counters at zero.  y is unspecified afterwards.  Nothing faults.
+ * the copies it did issue, and returns, leaving the context usable.  y is
+ * unspecified afterwards.  Nothing faults.
  */
 qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
                                      const void* packed, const void* x, const void* gate, const void* up,

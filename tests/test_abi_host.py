@@ -56,6 +56,8 @@ def test_version_and_status_strings(L):
     ("w4a8", 16, 1024, 512, qlin.ERR_UNSUPPORTED),
     ("w4a8", 24, 256, 32, qlin.ERR_UNSUPPORTED),   # N % 16
     ("w4a8", 16, 131072, 128, qlin.ERR_UNSUPPORTED),
+    ("w4a8", 16, 98304, 128, qlin.ERR_UNSUPPORTED),     # K beyond 16 CTAs x 4096
+    ("w6a8", 16, 65536, 256, qlin.OK),
     (7, 16, 256, 32, qlin.ERR_INVALID_ARG),
     ("w4a8", -16, 256, 32, qlin.ERR_INVALID_ARG),
     ("w4a8", 16, 0, 32, qlin.ERR_INVALID_ARG),

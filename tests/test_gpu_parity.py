@@ -32,12 +32,11 @@ def test_hand_example_exact(fmt):
     w = torch.from_numpy(wbuf).to(DEV)
     qlin.repack(w, fmt, N, K, G)
     x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).reshape(1, K).to(DEV)
-    y, acc = qlin.debug_group_acc(fmt, "none", w, N, K, G, x=x)
-    assert np.array_equal(y.cpu().numpy()[0], e["y"])
-    assert np.array_equal(acc.cpu().numpy()[0, :, 0], e["acc"])
-    q, s = qlin.debug_quantize_act(fmt, "none", K, G, x=x)
-    assert np.array_equal(q.cpu().numpy()[0].astype(np.int64), e["q"])
-    assert s.item() == e["s"]
+    r = qlin.debug_forward(fmt, "none", w, N, K, G, x=x)
+    assert np.array_equal(r["y"].cpu().numpy()[0], e["y"])
+    assert np.array_equal(r["acc"].cpu().numpy()[0, :, 0], e["acc"])
+    assert np.array_equal(r["q"].cpu().numpy()[0].astype(np.int64), e["q"])
+    assert r["s"].item() == e["s"]
     y2 = qlin.forward(fmt, "none", w, N, K, G, x=x)
     assert np.array_equal(y2.cpu().numpy()[0], e["y"])
 
@@ -76,10 +75,10 @@ def test_repack_twice_differs():
 def test_activation_codes(kind, M, K, G):
     c = inputs.make_case("w4a8", kind, M, 16, K, G, seed=M * 7 + K, outliers=0.01 if kind == "none" else 0.0)
     d = device_case(c)
-    q, s = qlin.debug_quantize_act("w4a8", kind, K, G, x=d["x"], gate=d["gate"], up=d["up"], gamma=d["gamma"],
-                                   eps=c.eps)
+    r = qlin.debug_forward("w4a8", kind, d["w"], 16, K, G, x=d["x"], gate=d["gate"], up=d["up"], gamma=d["gamma"],
+                           eps=c.eps)
     ref = oracle_forward(c)
-    qh, sh = q.cpu().numpy(), s.cpu().numpy()
+    qh, sh = r["q"].cpu().numpy(), r["s"].cpu().numpy()
     if kind == "none":
         assert np.array_equal(qh.astype(np.int64), ref["q"])
         assert np.array_equal(sh.astype(np.float64), ref["s"])
@@ -95,18 +94,17 @@ def test_activation_codes(kind, M, K, G):
 def test_group_sums_exact(fmt, kind, M, N, K, G):
     c = inputs.make_case(fmt, kind, M, N, K, G, seed=M + N + K)
     d = device_case(c)
-    y, acc = qlin.debug_group_acc(fmt, kind, d["w"], N, K, G, x=d["x"], gate=d["gate"], up=d["up"],
-                                  gamma=d["gamma"], eps=c.eps)
+    r = qlin.debug_forward(fmt, kind, d["w"], N, K, G, x=d["x"], gate=d["gate"], up=d["up"], gamma=d["gamma"],
+                           eps=c.eps)
+    y = r["y"]
     ref = oracle_forward(c)
-    acc_h = acc.cpu().numpy().astype(np.int64)
+    acc_h = r["acc"].cpu().numpy().astype(np.int64)
     if kind == "none":
         assert np.array_equal(acc_h, ref["acc"])
     else:
         # codes may legitimately differ at rounding boundaries; the sums must be
         # exact for the codes the GPU chose
-        q, _ = qlin.debug_quantize_act(fmt, kind, K, G, x=d["x"], gate=d["gate"], up=d["up"], gamma=d["gamma"],
-                                       eps=c.eps)
-        qg = q.cpu().numpy().astype(np.int64)
+        qg = r["q"].cpu().numpy().astype(np.int64)
         boundary_ok(qg, ref)
         dq = (qg - ref["q"]).reshape(M, K // G, G)
         codes, _ = O.unpack_file(fmt, N, K, G, c.wbuf.numpy())
@@ -195,10 +193,10 @@ def test_extreme_magnitudes_exact(fmt, code, sign):
     w = torch.from_numpy(O.pack_file(fmt, codes, sw)).to(DEV)
     qlin.repack(w, fmt, N, K, G)
     x = torch.full((8, K), sign, dtype=torch.bfloat16, device=DEV)
-    y, acc = qlin.debug_group_acc(fmt, "none", w, N, K, G, x=x)
+    r = qlin.debug_forward(fmt, "none", w, N, K, G, x=x)
     level = codes[0, 0] - (1 << (b - 1))
-    assert np.all(acc.cpu().numpy() == int(sign) * 127 * level * G)
-    assert np.all(y.cpu().numpy() == np.float32(sign * level * 2 * G))
+    assert np.all(r["acc"].cpu().numpy() == int(sign) * 127 * level * G)
+    assert np.all(r["y"].cpu().numpy() == np.float32(sign * level * 2 * G))
 
 
 def test_pdl_flag_same_result():
@@ -257,7 +255,7 @@ def test_device_timeout_is_reported_not_hung():
     c = inputs.make_case("w4a8", "none", 2, 512, 1024, 128, seed=9)
     d = device_case(c)
     ws = qlin.new_workspace(qlin.forward_workspace_bytes("w4a8", 512, 1024, 128))
-    st = qlin.debug_forward_fault("w4a8", "none", d["w"], 512, 1024, 128, unit=1, x=d["x"], ws=ws)
+    st = qlin.debug_forward_fault("w4a8", "none", d["w"], 512, 1024, 128, unit=0, x=d["x"], ws=ws)
     assert st == qlin.OK
     assert qlin.read_device_status(ws) == qlin.ERR_DEVICE_TIMEOUT
     qlin.workspace_init(ws)

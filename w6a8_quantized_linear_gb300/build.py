@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libqlin.so")
-SOURCES = [os.path.join(CSRC, f) for f in ("qlin_api.cu", "qlin_kernels.cuh", "qlin_layout.h", "qlin_ptx.cuh")] + [
+SOURCES = [os.path.join(CSRC, f) for f in ("qlin_api.cu", "qlin_forward.cuh", "qlin_repack.cuh", "qlin_layout.h", "qlin_ptx.cuh")] + [
     os.path.join(INCLUDE, "qlin.h")]
 
 

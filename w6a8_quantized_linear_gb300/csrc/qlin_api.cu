@@ -2,49 +2,38 @@
 //
 // Host-side planning: argument validation (shape rules from "Comfy
 // Quantization Formats", section "Format options", plus this backend's
-// limits), pipeline depth and grid size per device, workspace layout, and the
-// launches.  No allocation, no synchronisation (except the status read-back).
+// limits), the cluster size that splits K for each 256-row block, the
+// shared-memory carve, and the launches.  No allocation, no synchronisation
+// (except the status read-back).
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "qlin.h"
-#include "qlin_kernels.cuh"
+#include "qlin_forward.cuh"
+#include "qlin_repack.cuh"
 
 using namespace qlin;
 
 namespace {
 
-constexpr int64_t SMEM_BUDGET = 74 * 1024;  // per GEMV CTA: three CTAs share one SM
-
-struct KernelPlan {
-  int stages = 0;
-  int64_t stage_bytes = 0;
-  int64_t smem = 0;
-  int occ = 0;        // resident GEMV CTAs per SM
-  int64_t max_ctas = 0;
-};
+constexpr int64_t SMEM_TWO_PER_SM = 110 * 1024;  // dynamic bytes that leave room for a second CTA per SM
+constexpr int64_t SMEM_MAX = 225 * 1024;         // dynamic bytes of a CTA alone on its SM
 
 struct DevCache {
   bool init = false;
   int sms = 0;
-  KernelPlan plan[2][4];  // per (format, G index)
+  std::map<std::pair<int, int64_t>, int> clusters_ok;  // (C, smem) -> max active clusters (same for every kernel)
 };
 
 std::mutex g_mu;
 DevCache g_dev[64];
 
-int g_index(int64_t G) { return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : 3; }
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-
-template <int BITS>
-void* gemv_fn(bool debug) {
-  return debug ? reinterpret_cast<void*>(qlin_gemv_kernel<BITS, true>)
-               : reinterpret_cast<void*>(qlin_gemv_kernel<BITS, false>);
-}
 
 qlin_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return QLIN_OK;
@@ -52,77 +41,141 @@ qlin_status cuda_status(cudaError_t e) {
   return QLIN_ERR_CUDA;
 }
 
-// Pipeline depth, resident CTAs and the largest grid for (fmt, G) on the
-// current device.  All plans of a device are made at once, because the
-// dynamic shared memory limit is a property of the kernel function (shared by
-// every G): it is set to the largest stage area any plan of that function uses.
-constexpr int64_t GS[4] = {32, 64, 128, 256};
-constexpr int64_t PROLOGUE_SMEM_MAX = 64 * 1024;  // chunk of <= 12288 floats plus group sums
-
-qlin_status init_device(DevCache& c, int dev) {
-  cudaError_t e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return cuda_status(e);
-  for (int fi = 0; fi < 2; fi++) {
-    int64_t smem_max = 0;
-    for (int gi = 0; gi < 4; gi++) {
-      KernelPlan& pl = c.plan[fi][gi];
-      const Geo g = make_geo(fi, TILE_N, 256, GS[gi]);  // per-unit sizes only
-      pl.stage_bytes = round_up(g.bbf + g.unit_full, 128);
-      int64_t st = (SMEM_BUDGET - 128) / pl.stage_bytes;
-      if (st < 2) st = 2;
-      if (st > MAX_STAGES) st = MAX_STAGES;
-      pl.stages = (int)st;
-      pl.smem = pl.stages * pl.stage_bytes + 128;
-      if (pl.smem > smem_max) smem_max = pl.smem;
-    }
-    for (int dbg = 0; dbg < 2; dbg++) {
-      void* fn = fi == 1 ? gemv_fn<6>(dbg) : gemv_fn<4>(dbg);
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
-      if (e != cudaSuccess) return cuda_status(e);
-    }
-    for (int gi = 0; gi < 4; gi++) {
-      KernelPlan& pl = c.plan[fi][gi];
-      pl.occ = 0;
-      for (int dbg = 0; dbg < 2; dbg++) {
-        void* fn = fi == 1 ? gemv_fn<6>(dbg) : gemv_fn<4>(dbg);
-        int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, GEMV_THREADS, (size_t)pl.smem);
-        if (e != cudaSuccess) return cuda_status(e);
-        if (occ < 1) return QLIN_ERR_CUDA;
-        if (dbg == 0 || occ < pl.occ) pl.occ = occ;  // one grid for both, so debug runs match
-      }
-      pl.max_ctas = (int64_t)c.sms * pl.occ;
-    }
+template <int BITS, int KIND, int G>
+const void* fwd_fn() {
+  return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, KIND, G>);
+}
+template <int BITS, int KIND>
+const void* fwd_fn_g(int gi) {
+  switch (gi) {
+    case 0: return fwd_fn<BITS, KIND, 32>();
+    case 1: return fwd_fn<BITS, KIND, 64>();
+    case 2: return fwd_fn<BITS, KIND, 128>();
+    default: return fwd_fn<BITS, KIND, 256>();
   }
-  const void* pro[3] = {reinterpret_cast<const void*>(qlin_prologue_kernel<0>),
-                        reinterpret_cast<const void*>(qlin_prologue_kernel<1>),
-                        reinterpret_cast<const void*>(qlin_prologue_kernel<2>)};
-  for (const void* fn : pro) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PROLOGUE_SMEM_MAX);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
-  c.init = true;
-  return QLIN_OK;
+}
+int g_index(int64_t G) { return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : 3; }
+const void* forward_fn(int bits, int kind, int64_t G) {
+  const int gi = g_index(G);
+  if (bits == 6) return kind == 0 ? fwd_fn_g<6, 0>(gi) : kind == 1 ? fwd_fn_g<6, 1>(gi) : fwd_fn_g<6, 2>(gi);
+  return kind == 0 ? fwd_fn_g<4, 0>(gi) : kind == 1 ? fwd_fn_g<4, 1>(gi) : fwd_fn_g<4, 2>(gi);
 }
 
-qlin_status get_plan(int fmt, int64_t G, int* sms, KernelPlan* out) {
+// Per-device set-up: SM count, and the kernel attributes every launch relies on
+// (large dynamic shared memory, clusters of up to 16 CTAs).  Caller holds g_mu.
+qlin_status device_cache(DevCache** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_status(e);
   if (dev < 0 || dev >= 64) return QLIN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
   DevCache& c = g_dev[dev];
   if (!c.init) {
-    qlin_status st = init_device(c, dev);
-    if (st != QLIN_OK) return st;
+    e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    for (int bits : {4, 6})
+      for (int kind = 0; kind < 3; kind++)
+        for (int64_t G : {32, 64, 128, 256}) {
+          const void* fn = forward_fn(bits, kind, G);
+          e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
+          if (e != cudaSuccess) return cuda_status(e);
+          e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+          if (e != cudaSuccess) return cuda_status(e);
+        }
+    c.init = true;
   }
-  *sms = c.sms;
-  *out = c.plan[fmt == QLIN_W6A8 ? 1 : 0][g_index(G)];
+  *out = &c;
   return QLIN_OK;
 }
 
-qlin_status launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
-                   int cluster_x, bool pdl) {
+// How a forward call is laid out on the device.
+struct Plan {
+  int C = 1;          // CTAs per cluster: the split of K for one 256-row block
+  int64_t NB = 0;     // 256-row blocks (clusters)
+  int upc = 0;        // stream units per CTA, at most
+  int stages = 0;
+  int64_t stage_bytes = 0, b_off = 0, red_off = 0, smem = 0;
+};
+
+// Shared-memory carve: [stages][activation operand][split-K slots].  Fails
+// when the budget holds fewer than min_stages stages (or the CTA's units).
+bool carve(const Geo& g, Plan& pl, int64_t budget, int64_t min_stages) {
+  pl.stage_bytes = round_up(2 * g.unit_full, 128);
+  const int64_t b_bytes = round_up(pl.upc * g.bbf, 128);
+  const int64_t cmax = (CONSUMERS + pl.C - 1) / pl.C;
+  const int64_t red_bytes = round_up((int64_t)pl.C * cmax * 8 * 4, 128);
+  const int64_t rest = b_bytes + red_bytes + 128;
+  int64_t st = (budget - rest) / pl.stage_bytes;
+  if (st > MAX_STAGES) st = MAX_STAGES;
+  if (st > pl.upc) st = pl.upc;
+  if (st < (min_stages < pl.upc ? min_stages : pl.upc)) return false;
+  pl.stages = (int)st;
+  pl.b_off = pl.stages * pl.stage_bytes;
+  pl.red_off = pl.b_off + b_bytes;
+  pl.smem = pl.red_off + red_bytes + 128;
+  return true;
+}
+
+// Cluster size: as many CTAs per row block as fill two CTA slots per SM (16
+// consumer warps hide the latency of the unpack -> MMA chains), with the
+// fewest units on the busiest CTA; ties go to the smaller cluster.  K per CTA
+// is bounded by the shared-memory activation operand.  Caller holds g_mu.
+qlin_status make_plan(const Geo& g, DevCache& dc, int kind, Plan* out) {
+  Plan pl;
+  pl.NB = (g.T + TILES_PER_CTA - 1) / TILES_PER_CTA;
+  const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
+  const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
+  const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
+  if (cmin > cmax) return QLIN_ERR_UNSUPPORTED;
+  int64_t best = -1, best_upc = 0;
+  for (int64_t c = cmin; c <= cmax; c++) {
+    if (pl.NB * c > 2 * dc.sms) break;
+    const int64_t upc = (g.J + c - 1) / c;
+    if (best < 0 || upc < best_upc) {
+      best = c;
+      best_upc = upc;
+    }
+  }
+  if (best < 0) best = cmin;  // more blocks than slots: several waves
+  // the hardware must be able to co-schedule a cluster of this size
+  for (;; best--) {
+    pl.C = (int)best;
+    pl.upc = (int)((g.J + best - 1) / best);
+    bool fits = carve(g, pl, SMEM_TWO_PER_SM, 3) || carve(g, pl, SMEM_MAX, 2);
+    int n = 0;
+    if (fits) {
+      const auto key = std::make_pair((int)best, pl.smem);
+      auto it = dc.clusters_ok.find(key);
+      if (it == dc.clusters_ok.end()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)best, (unsigned)pl.NB, 1);
+        cfg.blockDim = dim3(GEMV_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)pl.smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = (unsigned)best;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, forward_fn(g.bits, kind, g.G), &cfg);
+        if (e != cudaSuccess) {
+          (void)cudaGetLastError();
+          n = 0;
+        }
+        dc.clusters_ok[key] = n;
+      } else {
+        n = it->second;
+      }
+    }
+    if (n >= 1) break;
+    if (best <= cmin) return QLIN_ERR_UNSUPPORTED;
+  }
+  *out = pl;
+  return QLIN_OK;
+}
+
+qlin_status launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args, int cluster_x,
+                   bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -130,13 +183,11 @@ qlin_status launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStrea
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
-  if (cluster_x > 0) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = cluster_x;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    na++;
-  }
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = cluster_x;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  na++;
   if (pdl) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
@@ -145,43 +196,6 @@ qlin_status launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStrea
   cfg.attrs = attr;
   cfg.numAttrs = na;
   return cuda_status(cudaLaunchKernelExC(&cfg, fn, args));
-}
-
-template <int KIND>
-const void* prologue_fn() {
-  return reinterpret_cast<const void*>(qlin_prologue_kernel<KIND>);
-}
-
-// Enqueue the prologue kernel: one cluster of CL CTAs per activation row.
-qlin_status launch_prologue(int fmt, int kind, int M, const Geo& g, const void* x, const void* gate, const void* up,
-                            const float* gamma, float eps, uint8_t* ws, uint32_t* tile_cnt, cudaStream_t s,
-                            bool pdl) {
-  ProParams p;
-  p.tile_cnt = tile_cnt;
-  p.T = g.T;
-  p.x = static_cast<const __nv_bfloat16*>(x);
-  p.gate = static_cast<const __nv_bfloat16*>(gate);
-  p.up = static_cast<const __nv_bfloat16*>(up);
-  p.gamma = gamma;
-  p.eps = eps;
-  p.ws = ws;
-  p.bits = bits_of(fmt);
-  p.K = g.K;
-  p.G = g.G;
-  p.KB = g.KB;
-  p.J = g.J;
-  p.bbf = g.bbf;
-  const int CL = (int)(g.J < 8 ? g.J : 8);
-  const int64_t chunk = (g.J + CL - 1) / CL * g.KB;
-  const size_t smem = (size_t)(round_up(chunk, 4) + chunk / g.G) * 4;
-  const void* fn = kind == QLIN_PROLOGUE_RMSNORM ? prologue_fn<1>() : kind == QLIN_PROLOGUE_SWIGLU ? prologue_fn<2>() : prologue_fn<0>();
-  if ((int64_t)smem > PROLOGUE_SMEM_MAX) return QLIN_ERR_UNSUPPORTED;
-  int sms = 0;
-  KernelPlan pl;
-  qlin_status st = get_plan(fmt, g.G, &sms, &pl);  // makes sure the device is initialised
-  if (st != QLIN_OK) return st;
-  void* args[] = {&p};
-  return launch(fn, dim3(CL, M, 1), dim3(PROLOGUE_THREADS, 1, 1), smem, s, args, CL, pdl);
 }
 
 qlin_status check_shape_impl(int fmt, int64_t N, int64_t K, int64_t G) {
@@ -197,9 +211,8 @@ qlin_status check_shape_impl(int fmt, int64_t N, int64_t K, int64_t G) {
   return QLIN_OK;
 }
 
-qlin_status check_act(int kind, int M, int64_t K, const void* x, const void* gate, const void* up,
-                      const float* gamma, float eps) {
-  (void)K;
+qlin_status check_act(int kind, int M, const void* x, const void* gate, const void* up, const float* gamma,
+                      float eps) {
   if (kind < 0 || kind > 2) return QLIN_ERR_INVALID_ARG;
   if (M < 0) return QLIN_ERR_INVALID_ARG;
   if (M > MAX_M) return QLIN_ERR_UNSUPPORTED;
@@ -215,64 +228,69 @@ qlin_status check_act(int kind, int M, int64_t K, const void* x, const void* gat
   return QLIN_OK;
 }
 
+struct Outputs {
+  float* y = nullptr;
+  int32_t* acc = nullptr;
+  int8_t* q = nullptr;
+  float* s = nullptr;
+};
+
 qlin_status forward_impl(int fmt, int kind, int M, int64_t N, int64_t K, int64_t G, const void* packed,
-                         const void* x, const void* gate, const void* up, const float* gamma, float eps, float* y,
-                         int32_t* acc, void* ws, size_t ws_bytes, unsigned flags, void* stream, bool debug,
+                         const void* x, const void* gate, const void* up, const float* gamma, float eps,
+                         const Outputs& out, void* ws, size_t ws_bytes, unsigned flags, void* stream, bool debug,
                          int64_t fault_unit = -1) {
   qlin_status st = check_shape_impl(fmt, N, K, G);
   if (st != QLIN_OK) return st;
-  st = check_act(kind, M, K, x, gate, up, gamma, eps);
+  st = check_act(kind, M, x, gate, up, gamma, eps);
   if (st != QLIN_OK) return st;
   if (flags & ~QLIN_FLAG_PDL) return QLIN_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return QLIN_OK;
   if (!packed || !aligned(packed, 16)) return QLIN_ERR_INVALID_ARG;
-  if (!debug && (!y || !aligned(y, 4))) return QLIN_ERR_INVALID_ARG;
-  if (y && !aligned(y, 4)) return QLIN_ERR_INVALID_ARG;
-  if (debug && (!acc || !aligned(acc, 4))) return QLIN_ERR_INVALID_ARG;
+  if (!debug && !out.y) return QLIN_ERR_INVALID_ARG;
+  if ((out.y && !aligned(out.y, 4)) || (out.acc && !aligned(out.acc, 4)) || (out.s && !aligned(out.s, 4)))
+    return QLIN_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return QLIN_ERR_INVALID_ARG;
-  int sms = 0;
-  KernelPlan pl;
-  st = get_plan(fmt, G, &sms, &pl);
-  if (st != QLIN_OK) return st;
+  if (ws_bytes < (size_t)WS_HEADER) return QLIN_ERR_WORKSPACE;
   const Geo g = make_geo(fmt, N, K, G);
-  const WsLayout wl = make_ws(g, pl.max_ctas);
-  if ((int64_t)ws_bytes < wl.total) return QLIN_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool pdl = (flags & QLIN_FLAG_PDL) != 0;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-
-  st = launch_prologue(fmt, kind, M, g, x, gate, up, gamma, eps, w, reinterpret_cast<uint32_t*>(w + wl.cnt_off), s,
-                       pdl);
-  if (st != QLIN_OK) return st;
-
-  GemvParams p;
+  Plan pl;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevCache* dc = nullptr;
+    st = device_cache(&dc);
+    if (st != QLIN_OK) return st;
+    st = make_plan(g, *dc, kind, &pl);
+    if (st != QLIN_OK) return st;
+  }
+  FwdParams p;
   p.packed = static_cast<const uint8_t*>(packed);
-  p.ws = w;
-  p.y = y;
-  p.acc_out = acc;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.gate = static_cast<const __nv_bfloat16*>(gate);
+  p.up = static_cast<const __nv_bfloat16*>(up);
+  p.gamma = gamma;
+  p.eps = eps;
+  p.y = out.y;
+  p.status = static_cast<uint32_t*>(ws);
+  p.acc_out = out.acc;
+  p.q_out = out.q;
+  p.s_out = out.s;
   p.M = M;
-  p.bits = g.bits;
   p.N = N;
   p.K = K;
-  p.G = G;
-  p.KB = g.KB;
   p.T = g.T;
   p.J = g.J;
-  p.U = g.U;
-  p.P = g.U < pl.max_ctas ? g.U : pl.max_ctas;
   p.tile_full = g.tile_full;
+  p.unit_full = g.unit_full;
   p.bbf = g.bbf;
   p.stage_bytes = pl.stage_bytes;
-  p.cnt_off = wl.cnt_off;
-  p.part_off = wl.part_off;
+  p.b_off = pl.b_off;
+  p.red_off = pl.red_off;
   p.stages = pl.stages;
   p.fault_unit = fault_unit;
-  const void* fn = g.bits == 6 ? gemv_fn<6>(debug) : gemv_fn<4>(debug);
+  (void)debug;
   void* args[] = {&p};
-  // Always allowed to overlap the prologue kernel it follows: the GEMV reads
-  // the activation operand only after griddepcontrol.wait.  Overlap with the
-  // kernels before the prologue is what QLIN_FLAG_PDL opts into.
-  return launch(fn, dim3((unsigned)p.P, 1, 1), dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, s, args, 0, true);
+  return launch(forward_fn(g.bits, kind, G), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
+                dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args, pl.C,
+                (flags & QLIN_FLAG_PDL) != 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -283,7 +301,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int64_t N, int64_t K, int64_t
 // synchronisation, or a deployment that fixes its memory footprint up
 // front).  They use this array instead of a caller-provided workspace.  Every
 // GPU that loads the library holds it until the process exits.
-constexpr size_t NOALLOC_SCRATCH_BYTES = 4u << 20;  // 4 MiB
+constexpr size_t NOALLOC_SCRATCH_BYTES = 64u << 10;  // 64 KiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_noalloc_mu;
@@ -311,7 +329,9 @@ qlin_status noalloc_scratch(void** out) {
 
 extern "C" {
 
-const char* qlin_version(void) { return "qlin 0.1 (sm_103a, bf16 mma.sync exact-integer path, TMA bulk stream)"; }
+const char* qlin_version(void) {
+  return "qlin 0.2 (sm_103a: fused prologue + TMA-streamed bf16 mma.sync GEMV, cluster split-K)";
+}
 
 const char* qlin_status_string(qlin_status s) {
   switch (s) {
@@ -404,11 +424,7 @@ qlin_status qlin_forward_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t 
   qlin_status st = check_shape_impl(fmt, N, K, G);
   if (st != QLIN_OK) return st;
   if (!bytes) return QLIN_ERR_INVALID_ARG;
-  int sms = 0;
-  KernelPlan pl;
-  st = get_plan(fmt, G, &sms, &pl);
-  if (st != QLIN_OK) return st;
-  *bytes = (size_t)make_ws(make_geo(fmt, N, K, G), pl.max_ctas).total;
+  *bytes = (size_t)WS_HEADER;
   return QLIN_OK;
 }
 
@@ -420,8 +436,10 @@ qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G, const void* packed,
                          const void* x, const void* gate, const void* up, const float* gamma, float eps, float* y,
                          void* ws, size_t ws_bytes, unsigned flags, void* stream) {
-  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, y, nullptr, ws, ws_bytes, flags,
-                      stream, false);
+  Outputs o;
+  o.y = y;
+  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, o, ws, ws_bytes, flags, stream,
+                      false);
 }
 
 qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, int64_t* ctas, int64_t* units,
@@ -429,13 +447,18 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, i
   qlin_status st = check_shape_impl(fmt, N, K, G);
   if (st != QLIN_OK) return st;
   if (!ctas || !units || !stream_bytes) return QLIN_ERR_INVALID_ARG;
-  int sms = 0;
-  KernelPlan pl;
-  st = get_plan(fmt, G, &sms, &pl);
-  if (st != QLIN_OK) return st;
   const Geo g = make_geo(fmt, N, K, G);
+  Plan pl;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevCache* dc = nullptr;
+    st = device_cache(&dc);
+    if (st != QLIN_OK) return st;
+    st = make_plan(g, *dc, QLIN_PROLOGUE_NONE, &pl);
+    if (st != QLIN_OK) return st;
+  }
+  *ctas = (int64_t)pl.C * pl.NB;
   *units = g.U;
-  *ctas = g.U < pl.max_ctas ? g.U : pl.max_ctas;
   *stream_bytes = (int64_t)qlin_packed_bytes(fmt, N, K, G);
   return QLIN_OK;
 }
@@ -449,30 +472,16 @@ qlin_status qlin_read_device_status(const void* ws, void* stream) {
   return (qlin_status)v;
 }
 
-qlin_status qlin_debug_quantize_act(int fmt, int prologue, int M, int64_t K, int64_t G, const void* x,
-                                    const void* gate, const void* up, const float* gamma, float eps, int8_t* q,
-                                    float* s, void* ws, size_t ws_bytes, void* stream) {
-  qlin_status st = check_shape_impl(fmt, 16, K, G);
-  if (st != QLIN_OK) return st;
-  st = check_act(prologue, M, K, x, gate, up, gamma, eps);
-  if (st != QLIN_OK) return st;
-  if (M == 0) return QLIN_OK;
-  if (!q || !s || !ws || !aligned(ws, 256)) return QLIN_ERR_INVALID_ARG;
-  const Geo g = make_geo(fmt, 16, K, G);
-  if ((int64_t)ws_bytes < make_ws(g, 0).cnt_off) return QLIN_ERR_WORKSPACE;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  st = launch_prologue(fmt, prologue, M, g, x, gate, up, gamma, eps, w, nullptr, cs, false);
-  if (st != QLIN_OK) return st;
-  qlin_debug_unpack_q_kernel<<<dim3(64, M), 256, 0, cs>>>(w, M, K, g.KB, g.bbf, q, s);
-  return cuda_status(cudaGetLastError());
-}
-
-qlin_status qlin_debug_group_acc(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G, const void* packed,
-                                 const void* x, const void* gate, const void* up, const float* gamma, float eps,
-                                 float* y, int32_t* acc, void* ws, size_t ws_bytes, void* stream) {
-  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, y, acc, ws, ws_bytes, 0, stream,
-                      true);
+qlin_status qlin_debug_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G, const void* packed,
+                               const void* x, const void* gate, const void* up, const float* gamma, float eps,
+                               float* y, int32_t* acc, int8_t* q, float* s, void* ws, size_t ws_bytes,
+                               void* stream) {
+  Outputs o;
+  o.y = y;
+  o.acc = acc;
+  o.q = q;
+  o.s = s;
+  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, o, ws, ws_bytes, 0, stream, true);
 }
 
 qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
@@ -480,8 +489,10 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
                                      const float* gamma, float eps, float* y, void* ws, size_t ws_bytes,
                                      int64_t unit, void* stream) {
   if (unit < 0) return QLIN_ERR_INVALID_ARG;
-  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, y, nullptr, ws, ws_bytes, 0, stream,
-                      false, unit);
+  Outputs o;
+  o.y = y;
+  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, o, ws, ws_bytes, 0, stream, false,
+                      unit);
 }
 
 qlin_status qlin_forward_noalloc(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
@@ -496,8 +507,10 @@ qlin_status qlin_forward_noalloc(int fmt, int prologue, int M, int64_t N, int64_
   void* ws = nullptr;
   st = noalloc_scratch(&ws);
   if (st != QLIN_OK) return st;
-  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, y, nullptr, ws,
-                      NOALLOC_SCRATCH_BYTES, flags, stream, false);
+  Outputs o;
+  o.y = y;
+  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, o, ws, NOALLOC_SCRATCH_BYTES, flags,
+                      stream, false);
 }
 
 }  // extern "C"

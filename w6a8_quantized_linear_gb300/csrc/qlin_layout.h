@@ -1,4 +1,4 @@
-// Geometry of the kernel-order weight stream and of the forward workspace.
+// Geometry of the kernel-order weight stream and of the fused forward kernel.
 // Shared by the host planner and the kernels of this library (one build).
 //
 // Stream: tiles of TILE_N = 128 output rows; in a tile, units of KB = max(128, G)
@@ -18,19 +18,22 @@
 
 namespace qlin {
 
-constexpr int TILE_N = 128;        // output rows per tile
+constexpr int TILE_N = 128;        // output rows per stream tile
 constexpr int SLAB = 16;           // rows of one tensor-core A tile
 constexpr int KSTEP = 16;          // k per bf16 MMA
 constexpr int PAIR_K = 32;         // two k-steps share one plane word pair
 constexpr int MAX_M = 8;           // rows of the activation (N side of the MMA)
-constexpr int CONSUMER_WARPS = 4;  // each owns two slabs (32 rows) of a tile
-constexpr int GEMV_THREADS = (CONSUMER_WARPS + 1) * 32;
+constexpr int TILES_PER_CTA = 2;   // a CTA owns a 256-row block: two stream tiles
+constexpr int ROWS_PER_CTA = TILES_PER_CTA * TILE_N;
+constexpr int CONSUMER_WARPS = 8;  // each owns two slabs (32 rows) of the block
+constexpr int CONSUMERS = CONSUMER_WARPS * 32;
+constexpr int GEMV_THREADS = CONSUMERS + 32;  // + one TMA producer warp
 constexpr int MAX_STAGES = 16;
-constexpr int WS_HEADER = 256;     // status word + row scales
-constexpr int WS_SCALE_OFF = 64;   // fp32 s[8] inside the header
-constexpr int PARTIAL_FLOATS = CONSUMER_WARPS * 32 * 8;  // one tile's split-K partial
-constexpr int PROLOGUE_THREADS = 256;
-constexpr int64_t MAX_K = 98304;
+constexpr int MAX_CLUSTER = 16;    // CTAs splitting K for one row block
+constexpr int64_t MAX_K_PER_CTA = 4096;  // activation operand held in shared memory
+constexpr int WS_HEADER = 256;     // forward workspace: status word (+ reserved)
+constexpr int YPART_FLOATS = CONSUMERS * 8;  // one CTA's split-K partial of its block
+constexpr int64_t MAX_K = (int64_t)MAX_CLUSTER * MAX_K_PER_CTA;
 
 QL_HD int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 QL_HD int64_t kb_of(int64_t G) { return G > 128 ? G : 128; }
@@ -83,22 +86,7 @@ QL_HD int64_t unit_offset(const Geo& g, int64_t t, int64_t j) {
   return t * g.tile_full + j * unit_bytes(g.bits, tile_rows(g, t), g.KB, g.G);
 }
 
-// Forward workspace layout: [header][activation blocks][tile counters][partials]
-struct WsLayout {
-  int64_t b_off, cnt_off, part_off, total;
-};
-QL_HD WsLayout make_ws(const Geo& g, int64_t max_ctas) {
-  WsLayout w;
-  w.b_off = WS_HEADER;
-  w.cnt_off = w.b_off + round_up(g.J * g.bbf, 256);
-  w.part_off = w.cnt_off + round_up(g.T * 4, 256);
-  w.total = w.part_off + max_ctas * 2 * PARTIAL_FLOATS * 4;
-  return w;
-}
-
-// Split of U units over P CTAs: CTA p owns [p*U/P, (p+1)*U/P).
-QL_HD int64_t split_begin(int64_t p, int64_t U, int64_t P) { return p * U / P; }
-// CTA owning unit x
-QL_HD int64_t split_owner(int64_t x, int64_t U, int64_t P) { return ((x + 1) * P - 1) / U; }
+// K split inside a cluster of C CTAs: rank c owns stream units [c*J/C, (c+1)*J/C).
+QL_HD int64_t split_begin(int64_t c, int64_t J, int64_t C) { return c * J / C; }
 
 }  // namespace qlin

@@ -58,10 +58,8 @@ def lib() -> ctypes.CDLL:
                 "qlin_forward_launch_info": (st, [i32, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                                   ctypes.POINTER(i64)]),
                 "qlin_read_device_status": (st, [vp, vp]),
-                "qlin_debug_quantize_act": (st, [i32, i32, i32, i64, i64, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp,
-                                                 sz, vp]),
-                "qlin_debug_group_acc": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
-                                              vp, sz, vp]),
+                "qlin_debug_forward": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                            vp, vp, vp, sz, vp]),
                 "qlin_debug_forward_fault": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp,
                                                   vp, sz, i64, vp]),
                 "qlin_forward_noalloc": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp,
@@ -195,34 +193,23 @@ def read_device_status(ws: torch.Tensor, stream=None) -> int:
     return lib().qlin_read_device_status(_ptr(ws), _stream(stream))
 
 
-def debug_quantize_act(fmt, prologue, K: int, G: int, x=None, gate=None, up=None, gamma=None, eps: float = 1e-6,
-                       ws: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+def debug_forward(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, x=None, gate=None, up=None,
+                  gamma=None, eps: float = 1e-6, ws: torch.Tensor | None = None, stream=None) -> dict:
+    """qlin_forward with its test exports: y, exact group sums, activation codes, row scales."""
     act = gate if _pro(prologue) == 2 else x
     M = act.shape[0]
-    dev = act.device
-    q = torch.empty(M, K, dtype=torch.int8, device=dev)
-    s = torch.empty(M, dtype=torch.float32, device=dev)
+    dev = packed.device
+    out = {"y": torch.empty(M, N, dtype=torch.float32, device=dev),
+           "acc": torch.empty(M, N, K // G, dtype=torch.int32, device=dev),
+           "q": torch.empty(M, K, dtype=torch.int8, device=dev),
+           "s": torch.empty(M, dtype=torch.float32, device=dev)}
     if ws is None:
-        ws = new_workspace(forward_workspace_bytes(fmt, 16, K, G), dev, stream)
-    _check(lib().qlin_debug_quantize_act(_fmt(fmt), _pro(prologue), M, K, G, _ptr(x), _ptr(gate), _ptr(up),
-                                         _ptr(gamma), float(eps), _ptr(q), _ptr(s), _ptr(ws), ws.numel(),
-                                         _stream(stream)), "debug_quantize_act")
-    return q, s
-
-
-def debug_group_acc(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, x=None, gate=None, up=None,
-                    gamma=None, eps: float = 1e-6, ws: torch.Tensor | None = None,
-                    stream=None) -> tuple[torch.Tensor, torch.Tensor]:
-    act = gate if _pro(prologue) == 2 else x
-    M = act.shape[0]
-    y = torch.empty(M, N, dtype=torch.float32, device=packed.device)
-    acc = torch.empty(M, N, K // G, dtype=torch.int32, device=packed.device)
-    if ws is None:
-        ws = new_workspace(forward_workspace_bytes(fmt, N, K, G), packed.device, stream)
-    _check(lib().qlin_debug_group_acc(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate),
-                                      _ptr(up), _ptr(gamma), float(eps), _ptr(y), _ptr(acc), _ptr(ws), ws.numel(),
-                                      _stream(stream)), "debug_group_acc")
-    return y, acc
+        ws = new_workspace(forward_workspace_bytes(fmt, N, K, G), dev, stream)
+    _check(lib().qlin_debug_forward(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate),
+                                    _ptr(up), _ptr(gamma), float(eps), _ptr(out["y"]), _ptr(out["acc"]),
+                                    _ptr(out["q"]), _ptr(out["s"]), _ptr(ws), ws.numel(), _stream(stream)),
+           "debug_forward")
+    return out
 
 
 def debug_forward_fault(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, unit: int, x=None, gate=None,
