@@ -8,8 +8,8 @@ down, none before o; codes uniform, scales ~ U(0.005, 0.02), activations
 all distinct, so every step streams them from HBM (inputs larger than L2).
 
 One step = the 448 qlin_forward calls of the stack at one M, replayed as one
-CUDA graph (each call = fused prologue kernel + GEMV kernel, launched with
-programmatic dependent launch).  value = weight bytes per step / step time at
+CUDA graph (each call is one cluster launch of the fused prologue + GEMV
+kernel, with programmatic dependent launch).  value = weight bytes per step / step time at
 M = 1; the same at M = 8 and t(M=8)/t(M=1) are reported alongside.
 
 --impl reference times the CPU oracle (the method's plain definition) on a
@@ -17,6 +17,10 @@ bounded sample of the same workload: one layer at M = 1.
 
 Multi-GPU: the path does not shard across GPUs in this benchmark; N ranks run
 N independent replicas (weak scaling), value = total bytes / max rank time.
+
+--linear NAME [--calls C] [--M m] runs C calls of one linear type of the stack
+(distinct weights), once, and prints their launch shape: a small, bounded
+command for profilers.
 """
 from __future__ import annotations
 
@@ -309,6 +313,47 @@ def run_reference(args):
     return 0
 
 
+def run_linear(args):
+    """C calls of one linear type of the stack (distinct weights), for profilers."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from w6a8_quantized_linear_gb300 import inputs, qlin
+    spec = {name: (kind, K, N) for name, kind, K, N in inputs.STACK_LAYER}
+    kind, K, N = spec[args.linear]
+    G = inputs.STACK_G
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    lo, hi = inputs.STACK_SCALES
+    ws = qlin.new_workspace(qlin.forward_workspace_bytes("w4a8", N, K, G), dev)
+    calls = []
+    for _ in range(args.calls):
+        ncb = N * K // 2
+        w = torch.empty(qlin.packed_bytes("w4a8", N, K, G), dtype=torch.uint8, device=dev)
+        w[:ncb] = torch.randint(0, 256, (ncb,), generator=g, dtype=torch.uint8, device=dev)
+        w[ncb:].view(torch.float32).uniform_(lo, hi, generator=g)
+        qlin.repack(w, "w4a8", N, K, G)
+        x = gate = up = gamma = None
+        if kind == "swiglu":
+            gate = torch.randn(args.M, K, generator=g, device=dev).to(torch.bfloat16)
+            up = torch.randn(args.M, K, generator=g, device=dev).to(torch.bfloat16)
+        else:
+            x = torch.randn(args.M, K, generator=g, device=dev).to(torch.bfloat16)
+        if kind == "rmsnorm":
+            gamma = torch.empty(K, device=dev).uniform_(0.5, 1.5, generator=g)
+        calls.append((w, x, gate, up, gamma, torch.empty(args.M, N, device=dev)))
+    for w, x, gate, up, gamma, y in calls:
+        qlin.forward("w4a8", kind, w, N, K, G, x=x, gate=gate, up=up, gamma=gamma, y=y, ws=ws, flags=qlin.FLAG_PDL)
+    torch.cuda.synchronize()
+    assert qlin.read_device_status(ws) == qlin.OK
+    print(json.dumps({"linear": args.linear, "M": args.M, "N": N, "K": K, "calls": args.calls,
+                      "launch": qlin.launch_info("w4a8", N, K, G)}))
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -318,9 +363,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--linear", default=None, help="profile mode: one linear type of the stack")
+    ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--M", type=int, default=1)
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.linear is not None:
+        return run_linear(args)
     if args.warmup < 3:
         args.warmup = 3
 
@@ -339,7 +389,7 @@ def main():
 
     g1, ncalls = stack.step_graph(1, stream)
     g8, _ = stack.step_graph(8, stream)
-    kernels_per_step = 2 * ncalls
+    kernels_per_step = ncalls
 
     with ClockSampler(local) as clk:
         t1 = time_graph(g1, stream, args.steps, args.warmup, world, dev)

@@ -209,19 +209,20 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
  * is for callers that cannot allocate device memory where they run the layer
  * (a host whose memory pool owns the whole device and forbids cudaMalloc, code
  * that must avoid cudaMalloc's implicit synchronisation, a fixed-footprint
- * deployment).  The call allocates nothing; it uses a 4 MiB device array
+ * deployment).  The call allocates nothing; it uses a 64 KiB device array
  * inside the library instead, which every GPU that loads the library holds
  * until the process exits.
  *  - Arguments are those of qlin_forward without ws/ws_bytes.
  *  - Returns QLIN_ERR_WORKSPACE when the shape's workspace
- *    (qlin_forward_workspace_bytes) exceeds 4 MiB; nothing is enqueued then.
+ *    (qlin_forward_workspace_bytes) exceeds 64 KiB; nothing is enqueued then.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any CUDA
  *    stream capture.
- *  - All calls share the one array, which keeps the previous call's contents;
- *    each call resets what must start at zero.  Calls that overlap on the GPU
- *    (different streams, or unordered work) race on it: order them on one
- *    stream.
+ *  - All calls share the one array, which keeps the previous call's contents.
+ *    The forward kernel keeps nothing there that must start at zero: the
+ *    array holds only the status word, written only when a wait expires.
+ *    Calls that overlap on the GPU (different streams, or unordered work)
+ *    race on it: order them on one stream.
  *  - A device-side wait that expires is recorded in the array's status word,
  *    which this entry point does not read back; the kernel still returns
  *    instead of hanging.

@@ -27,7 +27,7 @@ constexpr int64_t SMEM_MAX = 225 * 1024;         // dynamic bytes of a CTA alone
 struct DevCache {
   bool init = false;
   int sms = 0;
-  std::map<std::pair<int, int64_t>, int> clusters_ok;  // (C, smem) -> max active clusters (same for every kernel)
+  std::map<std::pair<std::pair<const void*, int>, int64_t>, int> clusters;  // (kernel, C, smem) -> max active clusters
 };
 
 std::mutex g_mu;
@@ -115,63 +115,62 @@ bool carve(const Geo& g, Plan& pl, int64_t budget, int64_t min_stages) {
   return true;
 }
 
-// Cluster size: as many CTAs per row block as fill two CTA slots per SM (16
-// consumer warps hide the latency of the unpack -> MMA chains), with the
-// fewest units on the busiest CTA; ties go to the smaller cluster.  K per CTA
-// is bounded by the shared-memory activation operand.  Caller holds g_mu.
+// Clusters of C CTAs (each with `smem` dynamic bytes) that the device holds at
+// once, from the occupancy query; cached per (kernel, C, smem).  Caller holds g_mu.
+int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
+  const auto key = std::make_pair(std::make_pair(fn, C), smem);
+  auto it = dc.clusters.find(key);
+  if (it != dc.clusters.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C, 1, 1);
+  cfg.blockDim = dim3(GEMV_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)C;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  dc.clusters[key] = n;
+  return n;
+}
+
+// Cluster size C, the split of K for one 256-row block.  For every C that the
+// shared-memory activation operand allows, the carve and the number of
+// clusters the device holds at once give the waves of the launch; the cost is
+// waves x stream units of the busiest CTA.  The cheapest C wins, ties going
+// to the smaller cluster.  Caller holds g_mu.
 qlin_status make_plan(const Geo& g, DevCache& dc, int kind, Plan* out) {
-  Plan pl;
-  pl.NB = (g.T + TILES_PER_CTA - 1) / TILES_PER_CTA;
+  const int64_t NB = (g.T + TILES_PER_CTA - 1) / TILES_PER_CTA;
   const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
   const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
   const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
   if (cmin > cmax) return QLIN_ERR_UNSUPPORTED;
-  int64_t best = -1, best_upc = 0;
+  const void* fn = forward_fn(g.bits, kind, g.G);
+  bool found = false;
+  int64_t best_cost = 0;
   for (int64_t c = cmin; c <= cmax; c++) {
-    if (pl.NB * c > 2 * dc.sms) break;
-    const int64_t upc = (g.J + c - 1) / c;
-    if (best < 0 || upc < best_upc) {
-      best = c;
-      best_upc = upc;
+    Plan pl;
+    pl.NB = NB;
+    pl.C = (int)c;
+    pl.upc = (int)((g.J + c - 1) / c);
+    if (!(carve(g, pl, SMEM_TWO_PER_SM, 3) || carve(g, pl, SMEM_MAX, 2))) continue;
+    const int n = active_clusters(dc, fn, pl.C, pl.smem);
+    if (n < 1) continue;
+    const int64_t cost = (NB + n - 1) / n * pl.upc;
+    if (!found || cost < best_cost) {
+      found = true;
+      best_cost = cost;
+      *out = pl;
     }
   }
-  if (best < 0) best = cmin;  // more blocks than slots: several waves
-  // the hardware must be able to co-schedule a cluster of this size
-  for (;; best--) {
-    pl.C = (int)best;
-    pl.upc = (int)((g.J + best - 1) / best);
-    bool fits = carve(g, pl, SMEM_TWO_PER_SM, 3) || carve(g, pl, SMEM_MAX, 2);
-    int n = 0;
-    if (fits) {
-      const auto key = std::make_pair((int)best, pl.smem);
-      auto it = dc.clusters_ok.find(key);
-      if (it == dc.clusters_ok.end()) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)best, (unsigned)pl.NB, 1);
-        cfg.blockDim = dim3(GEMV_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = (size_t)pl.smem;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = (unsigned)best;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, forward_fn(g.bits, kind, g.G), &cfg);
-        if (e != cudaSuccess) {
-          (void)cudaGetLastError();
-          n = 0;
-        }
-        dc.clusters_ok[key] = n;
-      } else {
-        n = it->second;
-      }
-    }
-    if (n >= 1) break;
-    if (best <= cmin) return QLIN_ERR_UNSUPPORTED;
-  }
-  *out = pl;
-  return QLIN_OK;
+  return found ? QLIN_OK : QLIN_ERR_UNSUPPORTED;
 }
 
 qlin_status launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args, int cluster_x,

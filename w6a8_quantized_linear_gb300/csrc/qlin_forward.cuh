@@ -11,7 +11,8 @@
 //   * eight consumer warps load the CTA's slice of the activations once
 //     (every load in flight together), compute the prologue and the per-row
 //     statistics, push the statistics into every peer CTA's shared memory
-//     (remote stores + remote mbarrier arrivals), combine the cluster's
+//     (asynchronous remote stores that complete on the peer's mbarrier as
+//     transaction bytes), combine the cluster's
 //     statistics in rank order (deterministic, independent of M), quantise
 //     their K range into a shared-memory bf16 operand, run the tensor-core
 //     group dot products, and push their split-K partial sums to the CTA
@@ -184,8 +185,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
   __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
-  __shared__ __align__(8) uint64_t stat_bar;  // one remote arrival per cluster rank: statistics pushed
-  __shared__ __align__(8) uint64_t red_bar;   // one remote arrival per cluster rank: partial sums pushed
+  __shared__ __align__(8) uint64_t stat_bar;  // completes when every rank's statistics have landed
+  __shared__ __align__(8) uint64_t red_bar;   // completes when every rank's partial sums have landed
   __shared__ float s_red[CONSUMER_WARPS][MAX_M][2];
   __shared__ __align__(16) float s_slot[MAX_CLUSTER][MAX_M][2];  // rank r's (amax, sum x^2) per row
   __shared__ float s_row[MAX_M][3];                               // s, 127 / amax, rstd
@@ -201,14 +202,21 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   const int64_t tA = rb * TILES_PER_CTA;
   const bool hasB = tA + 1 < p.T;
   const int S = p.stages;
+  const int M = p.M;
+  // split-K positions (consumer thread slots) this CTA owns and finishes
+  const int pos0 = (int)(crank * CONSUMERS / C), pos1 = (int)((crank + 1) * CONSUMERS / C);
 
   if (tid == 0) {
     for (int s = 0; s < S; s++) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], CONSUMER_WARPS);
     }
-    mbar_init(&stat_bar, (uint32_t)C);
-    mbar_init(&red_bar, (uint32_t)C);
+    mbar_init(&stat_bar, 1);
+    mbar_init(&red_bar, 1);
+    // the bytes the peers push: (amax, sum x^2) per row from every rank, and
+    // two float4 partials per owned position from every rank
+    mbar_arrive_expect_tx(&stat_bar, (uint32_t)(C * M * 8));
+    mbar_arrive_expect_tx(&red_bar, (uint32_t)(C * (pos1 - pos0) * 32));
     mbar_fence_init();
   }
   __syncthreads();
@@ -255,7 +263,6 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
 
   // -------------------------------------------------------------------- consumers
   pdl_wait();  // activations may be written by the previous kernel in the stream
-  const int M = p.M;
   uint8_t* bop = smem + p.b_off;  // activation operand blocks, one per unit of this CTA
   const int rounds = (int)((n8 + CONSUMERS - 1) / CONSUMERS);
 
@@ -300,18 +307,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       a = fmaxf(a, s_red[w][tid][0]);
       q = __fadd_rn(q, s_red[w][tid][1]);
     }
-    const uint32_t local = smem_u32(&s_slot[crank][tid][0]);
-    for (int r = 0; r < C; r++) {
-      uint32_t remote;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"((uint32_t)r));
-      dsmem_st_f2(remote, a, q);
-    }
-  }
-  consumer_bar();
-  if (tid < C) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(&stat_bar)), "r"((uint32_t)tid));
-    mbar_arrive_remote(remote);
+    const uint32_t local = smem_u32(&s_slot[crank][tid][0]), lbar = smem_u32(&stat_bar);
+    for (int r = 0; r < C; r++) st_async_f2(dsmem_addr_u32(local, r), a, q, dsmem_addr_u32(lbar, r));
   }
   if (!mbar_wait_cluster(&stat_bar, 0) && lane == 0) atomicExch(p.status, 4u);
   if (tid < M) {
@@ -371,7 +368,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
 #pragma unroll
           for (int t = 0; t < 4; t++) {
             const uint32_t lo = __float_as_uint(qf[2 * t]) >> 16, hi = __float_as_uint(qf[2 * t + 1]) & 0xffff0000u;
-            *reinterpret_cast<uint32_t*>(blk + pr * 512 + (4 * m + t) * 16 + step * 8 + half * 4) = lo | hi;
+            *reinterpret_cast<uint32_t*>(blk + pr * B_PAIR + (4 * m + t) * 16 + step * 8 + half * 4) = lo | hi;
           }
           if (p.q_out && rb == 0) {
 #pragma unroll
@@ -387,7 +384,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       }
       if (valid && (lane % SEG) == 0) {
         const int64_t W = min((int64_t)KB, p.K - (j0 + jl) * KB);
-        float* cin = reinterpret_cast<float*>(blk + W * 16 + (kin / G) * 32);
+        float* cin = reinterpret_cast<float*>(blk + (W / PAIR_K) * B_PAIR + (kin / G) * 32);
         float4 c0, c1;
         c0.x = 0 < M ? corr * rowsum[0] : 0.f;
         c0.y = 1 < M ? corr * rowsum[1] : 0.f;
@@ -432,12 +429,12 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
 #pragma unroll
       for (int gi = 0; gi < GPU; gi++) {
         if (gi < ng) {
-          const float2 ci = *reinterpret_cast<const float2*>(bblk + W * 16 + gi * 32 + tq * 8);
+          const float2 ci = *reinterpret_cast<const float2*>(bblk + (W / PAIR_K) * B_PAIR + gi * 32 + tq * 8);
           float a0[4], b0[4], a1[4], b1[4];
 #pragma unroll
           for (int pp = 0; pp < PPG; pp++) {
             const int pr = gi * PPG + pp;
-            const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * 512 + lane * 16);
+            const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * B_PAIR + lane * 16);
             slab_pair<BITS>(c0p + pr * PB, lane, bq, pp == 0, ci, a0, b0);
             if (has1) slab_pair<BITS>(c1p + pr * PB, lane, bq, pp == 0, ci, a1, b1);
           }
@@ -489,19 +486,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     float* red = reinterpret_cast<float*>(smem + p.red_off);  // [rank][cmax][8]
     const int owner = ((tid + 1) * C - 1) / CONSUMERS;
     const int o0 = owner * CONSUMERS / C;
-    uint32_t dst;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst)
-                 : "r"(smem_u32(red + ((int)crank * cmax + (tid - o0)) * 8)), "r"((uint32_t)owner));
-    dsmem_st_f4(dst, make_float4(yacc[0][0], yacc[0][1], yacc[0][2], yacc[0][3]));
-    dsmem_st_f4(dst + 16, make_float4(yacc[1][0], yacc[1][1], yacc[1][2], yacc[1][3]));
-    consumer_bar();
-    if (tid < C) {
-      uint32_t remote;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(&red_bar)), "r"((uint32_t)tid));
-      mbar_arrive_remote(remote);
-    }
+    const uint32_t dst = dsmem_addr_u32(smem_u32(red + ((int)crank * cmax + (tid - o0)) * 8), (uint32_t)owner);
+    const uint32_t rbar = dsmem_addr_u32(smem_u32(&red_bar), (uint32_t)owner);
+    st_async_f4(dst, make_float4(yacc[0][0], yacc[0][1], yacc[0][2], yacc[0][3]), rbar);
+    st_async_f4(dst + 16, make_float4(yacc[1][0], yacc[1][1], yacc[1][2], yacc[1][3]), rbar);
     if (!mbar_wait_cluster(&red_bar, 0) && lane == 0) atomicExch(p.status, 4u);
-    const int pos0 = (int)(crank * CONSUMERS / C), pos1 = (int)((crank + 1) * CONSUMERS / C);
     if (tid < pos1 - pos0 && p.y != nullptr) {
       const int pos = pos0 + tid;
       float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};

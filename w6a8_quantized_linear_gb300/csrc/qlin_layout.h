@@ -46,9 +46,13 @@ QL_HD int pair_bytes(int bits) { return bits == 6 ? 384 : 256; }
 QL_HD int64_t unit_bytes(int bits, int64_t R, int64_t W, int64_t G) {
   return R * (W / G) * 4 + R * W * bits / 8;
 }
-// bytes of the activation operand block for W columns: bf16 fragments, then
-// one float pair block (8 rows) of -(128 + offset) * sum(q) per group
-QL_HD int64_t bblock_bytes(int64_t W, int64_t G) { return W * 16 + (W / G) * 32; }
+// Activation operand block of one unit (shared memory only): per 32-wide k
+// pair, 32 lanes x 16 bytes of bf16 MMA B fragments, padded to B_PAIR bytes so
+// that the quantising threads' stores to consecutive pairs fall in different
+// banks; then 8 floats per group, the group's start value
+// -(128 + offset) * sum q for each row.
+constexpr int B_PAIR = 528;
+QL_HD int64_t bblock_bytes(int64_t W, int64_t G) { return (W / 32) * B_PAIR + (W / G) * 32; }
 
 struct Geo {
   int bits;

@@ -7,6 +7,11 @@
 namespace qlin {
 
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s: far beyond any legitimate wait
+// Waits on data that peer CTAs of the cluster push get a longer bound than any
+// delay a peer can build up before it pushes (at most one expired pipeline
+// wait, after which it skips its remaining waits).  So a receiver never gives
+// up, and exits, while a peer may still write into its shared memory.
+constexpr uint64_t WAIT_LIMIT_CLUSTER_NS = 4000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -85,9 +90,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // Split-phase cluster barrier (all threads of all CTAs of the cluster take
 // part in every phase; the .aligned forms are not used, so a warp may arrive
 // with diverged lanes).  arrive has release, wait acquire semantics.
@@ -98,40 +100,32 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank)
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
   return remote;
 }
-__device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ float2 dsmem_ld_f2(const void* local, uint32_t rank) {
+__device__ __forceinline__ uint32_t dsmem_addr_u32(uint32_t local, uint32_t rank) {
   uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote) : "memory");
-  return v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
 }
 
 // Relaxed arrive (no ordering), used once after the mbarriers are initialised.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
-// Remote (distributed shared memory) stores and mbarrier arrivals: push a
-// value into a peer CTA's shared memory, then signal that peer's barrier with
-// cluster-scope release semantics (orders this CTA's earlier pushes).
-__device__ __forceinline__ void dsmem_st_f2(uint32_t addr, float a, float b) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
-}
-__device__ __forceinline__ void dsmem_st_f4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-               "f"(v.w)
+// Asynchronous remote stores into a peer CTA's shared memory that complete
+// on that peer's mbarrier as transaction bytes: the receiver waits on its own
+// barrier (which expects the bytes), with no fence or separate arrival.
+__device__ __forceinline__ void st_async_f2(uint32_t addr, float a, float b, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(a), "f"(b), "r"(remote_bar)
                : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+               : "memory");
 }
-// Wait (acquire at cluster scope) for a barrier that peers arrive on remotely;
-// false after WAIT_LIMIT_NS.
+// Wait (acquire at cluster scope) for a barrier that peers complete remotely;
+// false after WAIT_LIMIT_CLUSTER_NS.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -147,7 +141,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   while (!mbar_try_wait_cluster(bar, parity)) {
-    if (global_timer() - t0 > WAIT_LIMIT_NS) return false;
+    if (global_timer() - t0 > WAIT_LIMIT_CLUSTER_NS) return false;
   }
   return true;
 }

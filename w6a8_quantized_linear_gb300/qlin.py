@@ -171,7 +171,7 @@ def forward_noalloc(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int,
                     gamma=None, eps: float = 1e-6, y: torch.Tensor | None = None, flags: int = 0,
                     stream=None) -> torch.Tensor:
     """``forward`` for callers that cannot allocate device memory: the library
-    uses its own fixed 4 MiB device array as the workspace (see qlin.h)."""
+    uses its own fixed 64 KiB device array as the workspace (see qlin.h)."""
     act = gate if _pro(prologue) == 2 else x
     M = act.shape[0]
     if y is None:
