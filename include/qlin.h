@@ -113,13 +113,16 @@ size_t qlin_packed_bytes(int fmt, int64_t N, int64_t K, int64_t G);
  *     code block   for each slab, for each pair of 16-wide k-steps:
  *                  4-bit plane: 32 lanes x {word for step A, word for step B};
  *                  6-bit codes only, then the 2-bit plane: 32 lanes x 1 word.
- *   A lane (g, t) = (lane / 4, lane % 4) holds the A operand of a 16x16 bf16
+ *   A lane (g, t) = (lane / 4, lane % 4) holds the A operand of a 16x16 fp16
  *   tensor-core tile: register i in 0..3 holds (row g, k 2t..2t+1),
  *   (row g+8, k 2t..2t+1), (row g, k 2t+8..2t+9), (row g+8, k 2t+8..2t+9).  In
  *   a 4-bit plane word, register i's two elements sit at bits 4i..4i+3 and
  *   16+4i..16+4i+3 (the low 4 bits of the code).  In the 2-bit plane word the
- *   top 2 bits of step A register i sit at bits 2i and 16+2i, those of step B
- *   at bits 8+2i and 24+2i.  Codes are stored unsigned (not offset).
+ *   top 2 bits of register i of step s (0 = A, 1 = B) sit at bits
+ *   8s + 2*(i / 2) + 4*(i % 2) and 16 above that (odd k).  So a row-g field
+ *   and its row-g+8 partner are 4 bits apart in both planes, and one shift of
+ *   the 2-bit word lines a pair up with its nibbles.  Codes are stored
+ *   unsigned (not offset).
  *
  * buf: device, 16-byte aligned, qlin_packed_bytes(fmt, N, K, G) bytes.
  * ws : device scratch, 256-byte aligned, at least *min_bytes from

@@ -303,8 +303,8 @@ def unpack_stream(fmt: str, N: int, K: int, G: int, buf) -> tuple[np.ndarray, np
     step B), then for 6-bit codes the 2-bit plane as 32 lanes x 1 word.  In a
     plane word of lane (g, t), A-register i's two elements sit at bits
     4i..4i+3 and 16+4i..16+4i+3 (low 4 bits of the code).  In the 2-bit plane
-    word the top 2 bits of step A register i sit at bits 2i and 16+2i, those
-    of step B at bits 8+2i and 24+2i.
+    word the top 2 bits of register i of step s (0 = A, 1 = B) sit at bits
+    8s + 2*(i // 2) + 4*(i % 2) and 16 more than that.
     """
     b = BITS[fmt]
     buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
@@ -315,7 +315,7 @@ def unpack_stream(fmt: str, N: int, K: int, G: int, buf) -> tuple[np.ndarray, np
     elem = np.arange(2)[None, None, None, :]
     step = np.arange(2)[None, :, None, None]
     nib_shift = (16 * elem + 4 * reg).astype(np.uint32)                 # [1,1,4,2]
-    hi_shift = (8 * step + 16 * elem + 2 * reg).astype(np.uint32)       # [1,2,4,2]
+    hi_shift = (8 * step + 16 * elem + 2 * (reg // 2) + 4 * (reg % 2)).astype(np.uint32)  # [1,2,4,2]
     codes = np.full((N, K), -1, dtype=np.int64)
     sw = np.full((N, K // G), np.nan, dtype=np.float32)
     pos = 0

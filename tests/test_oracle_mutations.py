@@ -29,7 +29,7 @@ MUTANTS = {
     "scale_matrix_transposed": ("sw.reshape(N_all, K // G)[rows]", "sw.reshape(K // G, N_all).T[rows]"),
     "row_scale_dropped": ("y64 = s[:, None] * (", "y64 = 1.0 * ("),
     "acc_sign_flipped": ("L = np.asarray(codes, dtype=np.int64) - code_offset(fmt)", "L = code_offset(fmt) - np.asarray(codes, dtype=np.int64)"),
-    "stream_hi_bits_moved": ("(8 * step + 16 * elem + 2 * reg)", "(8 * step + 16 * elem + 2 * (3 - reg))"),
+    "stream_hi_bits_moved": ("2 * (reg // 2) + 4 * (reg % 2))", "4 * (reg // 2) + 2 * (reg % 2))"),
     "stream_rows_g_g8_swapped": ("row = g + 8 * (reg % 2)", "row = g + 8 * (reg // 2)"),
     "stream_scale_pairs_transposed": ("f.transpose(1, 3, 2, 0)", "f.transpose(1, 2, 3, 0)"),
 }

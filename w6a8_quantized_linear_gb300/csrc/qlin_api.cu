@@ -329,7 +329,7 @@ qlin_status noalloc_scratch(void** out) {
 extern "C" {
 
 const char* qlin_version(void) {
-  return "qlin 0.2 (sm_103a: fused prologue + TMA-streamed bf16 mma.sync GEMV, cluster split-K)";
+  return "qlin 0.3 (sm_103a: fused prologue + TMA-streamed fp16 mma.sync GEMV, cluster split-K)";
 }
 
 const char* qlin_status_string(qlin_status s) {

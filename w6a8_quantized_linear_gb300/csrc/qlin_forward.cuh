@@ -14,7 +14,7 @@
 //     (asynchronous remote stores that complete on the peer's mbarrier as
 //     transaction bytes), combine the cluster's
 //     statistics in rank order (deterministic, independent of M), quantise
-//     their K range into a shared-memory bf16 operand, run the tensor-core
+//     their K range into a shared-memory fp16 operand, run the tensor-core
 //     group dot products, and push their split-K partial sums to the CTA
 //     that owns those rows, which adds them in rank order and writes y.
 // The prologue never writes its intermediate to global memory and costs no
@@ -23,14 +23,22 @@
 // SwiGLU before it; weights and group scales are streamed in the order the
 // kernel reads them; the M <= 8 rows sit on the 8-wide side of the MMA).
 //
-// Exactness of the bf16 route.  A weight code c (0 <= c < 64) ORed into the
-// mantissa of bf16 128.0 (0x4300) is the bf16 number 128 + c exactly, and an
-// int8 code q (|q| <= 127) is exact in bf16.  Every product and partial sum of
-// a group (G <= 256) is an integer of magnitude below 2^24, so the fp32
-// accumulation of the MMA is exact.  Each group's first MMA starts from
-// -(128 + offset) * sum_k q[m,k], which leaves exactly sum_k q * (c - offset).
+// Exactness of the fp16 positional route.  fp16 1024.0 (0x6400) has ten
+// mantissa bits of weight 1, 2, ..., 512.  A code c (0 <= c < 64) ORed into
+// mantissa bits 0..5 gives 1024 + c exactly; ORed into bits 4..9 it gives
+// 1024 + 16c exactly.  The stream places the codes of tile row g at nibble
+// positions that need no shift for the first form, and those of row g + 8 at
+// the next nibble up for the second, so one AND-OR makes each A register.
+// An int8 code q (|q| <= 127) is exact in fp16.  Each MMA chain covers one
+// 16-wide k-step of every 32-wide pair of a sub-group of at most 128 k, and
+// starts from -(1024 + offset) * sum q (row g) or -(1024 + 16 offset) * sum q
+// (row g + 8) over its own k; every partial sum is then an integer below
+// 2^24 in magnitude, so the fp32 accumulation is exact.  Row g ends at
+// sum q * (c - offset), row g + 8 at 16 times that; the factor 16 is removed
+// (exactly) after the scales are applied.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "qlin_layout.h"
@@ -38,7 +46,7 @@
 
 namespace qlin {
 
-constexpr uint32_t BF16X2_128 = 0x43004300u;  // bf16 128.0 in both halves
+constexpr uint32_t F16X2_1024 = 0x64006400u;  // fp16 1024.0 in both halves
 constexpr float RINT_MAGIC = 12582912.0f;     // 1.5 * 2^23: x + M - M rounds x to an integer, ties to even
 
 struct FwdParams {
@@ -130,59 +138,62 @@ struct ActSlice {
   }
 };
 
+// One 16-wide k-step of one slab: the four fp16 A registers.  w is the step's
+// 4-bit plane word; h01 / h23 are the 2-bit plane word shifted so that the top
+// bits of registers 0/1 (2/3) sit at bits 4..5 (row g) and 8..9 (row g + 8).
 template <int BITS>
-__device__ __forceinline__ void unpack_step(uint32_t w, uint32_t h, int step, uint32_t (&a)[4]) {
-  // 4-bit plane: register i's elements at bits 4i..4i+3 and 16+4i..16+4i+3
-  a[0] = (w & 0x000F000Fu) | BF16X2_128;
-  a[1] = ((w >> 4) & 0x000F000Fu) | BF16X2_128;
-  a[2] = ((w >> 8) & 0x000F000Fu) | BF16X2_128;
-  a[3] = ((w >> 12) & 0x000F000Fu) | BF16X2_128;
+__device__ __forceinline__ void unpack_step(uint32_t w, uint32_t h01, uint32_t h23, uint32_t (&a)[4]) {
+  const uint32_t w8 = w >> 8;
+  a[0] = (w & 0x000F000Fu) | F16X2_1024;   // row g:     1024 + c
+  a[1] = (w & 0x00F000F0u) | F16X2_1024;   // row g + 8: 1024 + 16 c
+  a[2] = (w8 & 0x000F000Fu) | F16X2_1024;
+  a[3] = (w8 & 0x00F000F0u) | F16X2_1024;
   if (BITS == 6) {
-    // 2-bit plane: step A register i at bits 2i, 16+2i; step B at 8+2i, 24+2i;
-    // moved to bits 4..5 and 20..21 of the bf16 halves
-    if (step == 0) {
-      a[0] |= (h << 4) & 0x00300030u;
-      a[1] |= (h << 2) & 0x00300030u;
-      a[2] |= h & 0x00300030u;
-      a[3] |= (h >> 2) & 0x00300030u;
-    } else {
-      a[0] |= (h >> 4) & 0x00300030u;
-      a[1] |= (h >> 6) & 0x00300030u;
-      a[2] |= (h >> 8) & 0x00300030u;
-      a[3] |= (h >> 10) & 0x00300030u;
-    }
+    a[0] |= h01 & 0x00300030u;
+    a[1] |= h01 & 0x03000300u;
+    a[2] |= h23 & 0x00300030u;
+    a[3] |= h23 & 0x03000300u;
   }
 }
 
 // One 32-wide k pair of one 16-row slab: step A into chain ca, step B into cb.
-// The first pair of a group starts chain A at the group's offset correction
-// and chain B at zero.
+// The first pair of a sub-group starts each chain at its start value.
 template <int BITS>
-__device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uint4& bq, bool first, float2 ci,
-                                          float (&ca)[4], float (&cb)[4]) {
+__device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uint4& bq, bool first, const float4& sA,
+                                          const float4& sB, float (&ca)[4], float (&cb)[4]) {
   const uint2 w = *reinterpret_cast<const uint2*>(cp + lane * 8);
-  const uint32_t h = BITS == 6 ? *reinterpret_cast<const uint32_t*>(cp + 256 + lane * 4) : 0u;
+  uint32_t hA01 = 0, hA23 = 0, hB01 = 0, hB23 = 0;
+  if (BITS == 6) {
+    const uint32_t h = *reinterpret_cast<const uint32_t*>(cp + 256 + lane * 4);
+    hA01 = h << 4;
+    hA23 = h << 2;
+    hB01 = h >> 4;
+    hB23 = h >> 6;
+  }
   uint32_t a[4], b[4];
-  unpack_step<BITS>(w.x, h, 0, a);
-  unpack_step<BITS>(w.y, h, 1, b);
+  unpack_step<BITS>(w.x, hA01, hA23, a);
+  unpack_step<BITS>(w.y, hB01, hB23, b);
   if (first) {
-    mma_bf16_16816_c(ca, a[0], a[1], a[2], a[3], bq.x, bq.y, ci.x, ci.y, ci.x, ci.y);
-    mma_bf16_16816_c(cb, b[0], b[1], b[2], b[3], bq.z, bq.w, 0.f, 0.f, 0.f, 0.f);
+    mma_f16_16816_c(ca, a[0], a[1], a[2], a[3], bq.x, bq.y, sA.x, sA.y, sA.z, sA.w);
+    mma_f16_16816_c(cb, b[0], b[1], b[2], b[3], bq.z, bq.w, sB.x, sB.y, sB.z, sB.w);
   } else {
-    mma_bf16_16816(ca, a[0], a[1], a[2], a[3], bq.x, bq.y);
-    mma_bf16_16816(cb, b[0], b[1], b[2], b[3], bq.z, bq.w);
+    mma_f16_16816(ca, a[0], a[1], a[2], a[3], bq.x, bq.y);
+    mma_f16_16816(cb, b[0], b[1], b[2], b[3], bq.z, bq.w);
   }
 }
 
 template <int BITS, int KIND, int G>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
   constexpr int KB = G > 128 ? G : 128;  // k per stream unit
-  constexpr int PPG = G / PAIR_K;        // 32-wide pairs per group
+  constexpr int SG = G < 128 ? G : 128;  // k per MMA sub-group (exact chains)
+  constexpr int SPG = G / SG;            // sub-groups per group
   constexpr int GPU = KB / G;            // groups per full unit
-  constexpr int SEG = G / 8;             // lanes whose 8 k make one group (quantisation pass)
+  constexpr int PPS = SG / PAIR_K;       // 32-wide pairs per sub-group
+  constexpr int SEG = SG / 8;            // lanes whose 8 k make one sub-group (quantisation pass)
   constexpr int PB = BITS == 6 ? 384 : 256;
+  constexpr int CIN = (KB / PAIR_K) * B_PAIR;  // start values after the fragments of a block
 
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
   __shared__ __align__(8) uint64_t empty_bar[MAX_STAGES];
   __shared__ __align__(8) uint64_t stat_bar;  // completes when every rank's statistics have landed
@@ -191,8 +202,14 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   __shared__ __align__(16) float s_slot[MAX_CLUSTER][MAX_M][2];  // rank r's (amax, sum x^2) per row
   __shared__ float s_row[MAX_M][3];                               // s, 127 / amax, rstd
 
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // TMA destinations and vector loads need 16-byte alignment of the dynamic
+  // shared memory.  The layout is the same in every CTA of the launch, so
+  // either all CTAs leave here (before any barrier) or none does.
+  if ((smem_u32(smem) & 15u) != 0) {
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicExch(p.status, 3u);
+    return;
+  }
   const uint32_t crank = cluster_ctarank();
   const int C = (int)gridDim.x;
   const int64_t rb = blockIdx.y;
@@ -234,10 +251,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       const int64_t strideA = unit_bytes(BITS, RA, KB, G), strideB = unit_bytes(BITS, RB, KB, G);
       const bool fault_cta = blockIdx.x == 0 && blockIdx.y == 0;
       bool ok = true;
-      int issued = 0;
+      int issued = 0, s = 0;
+      uint32_t ph = 0;
       for (int i = 0; i < nu; i++) {
-        const int s = i % S;
-        if (i >= S && !mbar_wait(&empty_bar[s], (uint32_t)((i / S) - 1) & 1u)) {
+        if (i >= S && !mbar_wait(&empty_bar[s], ph ^ 1u)) {
           ok = false;
           break;
         }
@@ -247,9 +264,14 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         uint8_t* st = smem + (int64_t)s * p.stage_bytes;
         mbar_arrive_expect_tx(&full_bar[s], wa + wb);
         issued = i + 1;
-        if (fault_cta && i == p.fault_unit) continue;  // test only: this phase never completes
-        tma_load_1d(st, srcA + j * strideA, wa, &full_bar[s], pol);
-        if (hasB) tma_load_1d(st + p.unit_full, srcB + j * strideB, wb, &full_bar[s], pol);
+        if (!(fault_cta && i == p.fault_unit)) {  // test only: this phase never completes
+          tma_load_1d(st, srcA + j * strideA, wa, &full_bar[s], pol);
+          if (hasB) tma_load_1d(st + p.unit_full, srcB + j * strideB, wb, &full_bar[s], pol);
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (!ok) atomicExch(p.status, 4u);
       // every copy issued lands before the CTA may exit (in a normal run these
@@ -330,153 +352,176 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   }
   consumer_bar();
 
-  // ---- phase 2: quantise this CTA's K range into the MMA B operand (bf16)
-  //      plus each group's start value -(128 + offset) * sum q
+  // ---- phase 2: quantise this CTA's K range into the MMA B operand (fp16),
+  //      plus each sub-group's chain start values.  Every block is written
+  //      over its full width: past K the codes are zero, so a narrower last
+  //      unit contributes exactly nothing from the k it does not have.
   {
-    const float corr = -(float)(128 + code_offset(BITS));
-    for (int r = 0; r < rounds; r++) {
+    const float off = (float)code_offset(BITS);
+    const float fg = -(1024.0f + off), fg8 = -(1024.0f + 16.0f * off);  // rows g and g + 8
+    const int64_t n8f = (int64_t)nu * (KB / 8);
+    const int rounds2 = (int)((n8f + CONSUMERS - 1) / CONSUMERS);
+    for (int r = 0; r < rounds2; r++) {
       const int64_t i8 = (int64_t)r * CONSUMERS + tid;
-      const bool valid = i8 < n8;
+      const bool inb = i8 < n8f, valid = i8 < n8;
       if (valid && rounds > 1) act.load(p, M, k_lo + i8 * 8);
-      const int64_t kl = i8 * 8, jl = kl / KB, kin = kl - jl * KB;
+      const int64_t kl = i8 * 8, jl = kl / KB;
+      const int kin = (int)(kl - jl * KB);
       uint8_t* blk = bop + jl * p.bbf;
-      const int64_t pr = kin / PAIR_K;
-      const int step = (int)((kin / KSTEP) & 1), half = (int)((kin % KSTEP) >= 8);
+      const int pr = kin / PAIR_K, step = (kin / KSTEP) & 1, half = (kin % KSTEP) >= 8;
       float rowsum[MAX_M];
 #pragma unroll
       for (int m = 0; m < MAX_M; m++) {
         rowsum[m] = 0.f;
-        if (valid && m < M) {
-          float v[8], ss = 0.f;
-          act.value(m, v, ss);
-          const float s = s_row[m][0], mul = s_row[m][1], rs = s_row[m][2];
+        if (inb && m < M) {
           float qf[8];
+          if (valid) {
+            float v[8], ss = 0.f;
+            act.value(m, v, ss);
+            const float s = s_row[m][0], mul = s_row[m][1], rs = s_row[m][2];
 #pragma unroll
-          for (int e = 0; e < 8; e++) {
-            float t;
-            if (KIND == 0) {
-              t = s > 0.f ? __fdiv_rn(v[e], s) : 0.f;  // IEEE division: codes identical to the definition
-            } else {
-              const float a = KIND == 1 ? __fmul_rn(v[e], rs) : v[e];
-              t = __fmul_rn(a, mul);
+            for (int e = 0; e < 8; e++) {
+              float t;
+              if (KIND == 0) {
+                t = s > 0.f ? __fdiv_rn(v[e], s) : 0.f;  // IEEE division: codes identical to the definition
+              } else {
+                const float a = KIND == 1 ? __fmul_rn(v[e], rs) : v[e];
+                t = __fmul_rn(a, mul);
+              }
+              float q = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);  // round half to even
+              q = fminf(fmaxf(q, -127.0f), 127.0f);
+              qf[e] = q;
+              rowsum[m] += q;
             }
-            float q = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);  // round half to even
-            q = fminf(fmaxf(q, -127.0f), 127.0f);
-            qf[e] = q;
-            rowsum[m] += q;
+            if (p.q_out && rb == 0) {
+#pragma unroll
+              for (int e = 0; e < 8; e++) p.q_out[(int64_t)m * p.K + k_lo + kl + e] = (int8_t)(int)qf[e];
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++) qf[e] = 0.f;
           }
 #pragma unroll
           for (int t = 0; t < 4; t++) {
-            const uint32_t lo = __float_as_uint(qf[2 * t]) >> 16, hi = __float_as_uint(qf[2 * t + 1]) & 0xffff0000u;
-            *reinterpret_cast<uint32_t*>(blk + pr * B_PAIR + (4 * m + t) * 16 + step * 8 + half * 4) = lo | hi;
-          }
-          if (p.q_out && rb == 0) {
-#pragma unroll
-            for (int e = 0; e < 8; e++) p.q_out[(int64_t)m * p.K + k_lo + kl + e] = (int8_t)(int)qf[e];
+            const __half2 h2 = __floats2half2_rn(qf[2 * t], qf[2 * t + 1]);  // exact: |q| <= 127
+            *reinterpret_cast<__half2*>(blk + pr * B_PAIR + (4 * m + t) * 16 + step * 8 + half * 4) = h2;
           }
         }
       }
-      // lanes [SEG*i, SEG*(i+1)) hold one group's 8-k slices: add their sums
+      // lanes [SEG*i, SEG*(i+1)) hold one sub-group's 8-k slices; lane bit 1
+      // is the k-step, so summing over the other bits gives each chain's sum
 #pragma unroll
       for (int m = 0; m < MAX_M; m++) {
 #pragma unroll
-        for (int o = 1; o < SEG; o <<= 1) rowsum[m] += __shfl_xor_sync(0xffffffffu, rowsum[m], o);
+        for (int o = 1; o < SEG; o <<= 1)
+          if (o != 2) rowsum[m] += __shfl_xor_sync(0xffffffffu, rowsum[m], o);
       }
-      if (valid && (lane % SEG) == 0) {
-        const int64_t W = min((int64_t)KB, p.K - (j0 + jl) * KB);
-        float* cin = reinterpret_cast<float*>(blk + (W / PAIR_K) * B_PAIR + (kin / G) * 32);
-        float4 c0, c1;
-        c0.x = 0 < M ? corr * rowsum[0] : 0.f;
-        c0.y = 1 < M ? corr * rowsum[1] : 0.f;
-        c0.z = 2 < M ? corr * rowsum[2] : 0.f;
-        c0.w = 3 < M ? corr * rowsum[3] : 0.f;
-        c1.x = 4 < M ? corr * rowsum[4] : 0.f;
-        c1.y = 5 < M ? corr * rowsum[5] : 0.f;
-        c1.z = 6 < M ? corr * rowsum[6] : 0.f;
-        c1.w = 7 < M ? corr * rowsum[7] : 0.f;
-        reinterpret_cast<float4*>(cin)[0] = c0;
-        reinterpret_cast<float4*>(cin)[1] = c1;
+      if (inb && (lane % SEG) < 4 && (lane & 1) == 0) {
+        const int chain = (lane >> 1) & 1;
+        float* cin = reinterpret_cast<float*>(blk + CIN + (kin / SG) * 128 + chain * 64);
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+          const float s0 = 2 * t < M ? rowsum[2 * t] : 0.f;
+          const float s1 = 2 * t + 1 < M ? rowsum[2 * t + 1] : 0.f;
+          reinterpret_cast<float4*>(cin)[t] = make_float4(fg * s0, fg * s1, fg8 * s0, fg8 * s1);
+        }
       }
     }
   }
   consumer_bar();
 
-  // ---- phase 3: stream the weights through the tensor cores
+  // ---- phase 3: stream the weights through the tensor cores.  Every warp
+  //      runs its two slabs through every sub-group of every unit without a
+  //      data-dependent branch; slabs past a short tile, and groups past a
+  //      narrower last unit, compute from in-bounds shared memory and are
+  //      dropped (their scale is zeroed, their rows are never written).
   const int g = lane >> 2, tq = lane & 3;
   const int tsel = warp >> 2;  // which of the CTA's two tiles this warp works on
   const int64_t t = tA + tsel;
-  const int64_t R = (tsel == 0 || hasB) ? min((int64_t)TILE_N, p.N - t * TILE_N) : 0;
-  const int nslab = (int)(R / SLAB);
+  const int R = (tsel == 0 || hasB) ? (int)min((int64_t)TILE_N, p.N - t * TILE_N) : 0;
+  const int nslab = R / SLAB;
   const int sl0 = 2 * (warp & 3);
-  const bool has0 = sl0 < nslab, has1 = sl0 + 1 < nslab;
-  bool ok = true;
+  const int W_last = (int)(p.K - (p.J - 1) * KB);
+  const uint8_t* tile_base = smem + tsel * p.unit_full;
   float yacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  int s = 0;
+  uint32_t ph = 0;
 
   for (int i = 0; i < nu; i++) {
-    const int s = i % S;
-    if (ok && !mbar_wait(&full_bar[s], (uint32_t)(i / S) & 1u)) {
-      ok = false;
+    if (!mbar_wait(&full_bar[s], ph)) {
+      // A timeout leaves this stage unreleased: the producer's own bounded wait
+      // then expires instead of re-arming a barrier that is still pending.
       if (lane == 0) atomicExch(p.status, 4u);
+      break;
     }
-    if (ok && has0) {
-      const int64_t j = j0 + i, W = min((int64_t)KB, p.K - j * KB);
-      const int ng = (int)(W / G);
-      const uint8_t* unit = smem + (int64_t)s * p.stage_bytes + tsel * p.unit_full;
-      const float* scl = reinterpret_cast<const float*>(unit);
-      const uint8_t* c0p = unit + R * ng * 4 + sl0 * (2 * BITS * W);
-      const uint8_t* c1p = c0p + 2 * BITS * W;
-      const uint8_t* bblk = bop + (int64_t)i * p.bbf;
+    const int W = (j0 + i == p.J - 1) ? W_last : KB;
+    const int ng = W / G;
+    const int slab_bytes = (W / PAIR_K) * PB;
+    const uint8_t* unit = tile_base + (int64_t)s * p.stage_bytes;
+    const float* scl = reinterpret_cast<const float*>(unit);
+    const uint8_t* c0p = unit + R * ng * 4 + sl0 * slab_bytes;
+    const uint8_t* c1p = c0p + slab_bytes;
+    const uint8_t* bblk = bop + (int64_t)i * p.bbf;
 #pragma unroll
-      for (int gi = 0; gi < GPU; gi++) {
-        if (gi < ng) {
-          const float2 ci = *reinterpret_cast<const float2*>(bblk + (W / PAIR_K) * B_PAIR + gi * 32 + tq * 8);
-          float a0[4], b0[4], a1[4], b1[4];
+    for (int gi = 0; gi < GPU; gi++) {
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int pp = 0; pp < PPG; pp++) {
-            const int pr = gi * PPG + pp;
-            const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * B_PAIR + lane * 16);
-            slab_pair<BITS>(c0p + pr * PB, lane, bq, pp == 0, ci, a0, b0);
-            if (has1) slab_pair<BITS>(c1p + pr * PB, lane, bq, pp == 0, ci, a1, b1);
-          }
-          float d0[4], d1[4];
+      for (int h = 0; h < SPG; h++) {
+        const int sg = gi * SPG + h;
+        const float4 sA = *reinterpret_cast<const float4*>(bblk + CIN + sg * 128 + tq * 16);
+        const float4 sB = *reinterpret_cast<const float4*>(bblk + CIN + sg * 128 + 64 + tq * 16);
+        float a0[4], b0[4], a1[4], b1[4];
 #pragma unroll
-          for (int e = 0; e < 4; e++) {  // exact: integer sums below 2^24
-            d0[e] = a0[e] + b0[e];
-            d1[e] = has1 ? a1[e] + b1[e] : 0.f;
-          }
-          const float2 sw0 = *reinterpret_cast<const float2*>(scl + (gi * nslab + sl0) * 16 + 2 * g);
-          yacc[0][0] = __fmaf_rn(sw0.x, d0[0], yacc[0][0]);
-          yacc[0][1] = __fmaf_rn(sw0.x, d0[1], yacc[0][1]);
-          yacc[0][2] = __fmaf_rn(sw0.y, d0[2], yacc[0][2]);
-          yacc[0][3] = __fmaf_rn(sw0.y, d0[3], yacc[0][3]);
-          if (has1) {
-            const float2 sw1 = *reinterpret_cast<const float2*>(scl + (gi * nslab + sl0 + 1) * 16 + 2 * g);
-            yacc[1][0] = __fmaf_rn(sw1.x, d1[0], yacc[1][0]);
-            yacc[1][1] = __fmaf_rn(sw1.x, d1[1], yacc[1][1]);
-            yacc[1][2] = __fmaf_rn(sw1.y, d1[2], yacc[1][2]);
-            yacc[1][3] = __fmaf_rn(sw1.y, d1[3], yacc[1][3]);
-          }
-          if (p.acc_out) {  // test export: exact group sums
-            const int64_t NG = p.K / G, gg = (j * KB) / G + gi;
+        for (int pp = 0; pp < PPS; pp++) {
+          const int pr = sg * PPS + pp;
+          const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * B_PAIR + lane * 16);
+          slab_pair<BITS>(c0p + pr * PB, lane, bq, pp == 0, sA, sB, a0, b0);
+          slab_pair<BITS>(c1p + pr * PB, lane, bq, pp == 0, sA, sB, a1, b1);
+        }
 #pragma unroll
-            for (int a = 0; a < 2; a++) {
-              if (a == 1 && !has1) continue;
-              const float* d = a == 0 ? d0 : d1;
-              const int64_t n0 = t * TILE_N + (sl0 + a) * SLAB + g;
+        for (int e = 0; e < 4; e++) {  // exact: integer sums below 2^24
+          d0[e] += a0[e] + b0[e];
+          d1[e] += a1[e] + b1[e];
+        }
+      }
+      float2 sw0 = *reinterpret_cast<const float2*>(scl + (gi * nslab + sl0) * 16 + 2 * g);
+      float2 sw1 = *reinterpret_cast<const float2*>(scl + (gi * nslab + sl0 + 1) * 16 + 2 * g);
+      if (GPU > 1 && gi >= ng) sw0 = sw1 = make_float2(0.f, 0.f);  // group past a narrower unit
+      yacc[0][0] = __fmaf_rn(sw0.x, d0[0], yacc[0][0]);
+      yacc[0][1] = __fmaf_rn(sw0.x, d0[1], yacc[0][1]);
+      yacc[0][2] = __fmaf_rn(sw0.y, d0[2], yacc[0][2]);
+      yacc[0][3] = __fmaf_rn(sw0.y, d0[3], yacc[0][3]);
+      yacc[1][0] = __fmaf_rn(sw1.x, d1[0], yacc[1][0]);
+      yacc[1][1] = __fmaf_rn(sw1.x, d1[1], yacc[1][1]);
+      yacc[1][2] = __fmaf_rn(sw1.y, d1[2], yacc[1][2]);
+      yacc[1][3] = __fmaf_rn(sw1.y, d1[3], yacc[1][3]);
+      if (p.acc_out && gi < ng) {  // test export: exact group sums
+        const int64_t NG = p.K / G, gg = ((j0 + i) * KB) / G + gi;
 #pragma unroll
-              for (int e = 0; e < 4; e++) {
-                const int mm = 2 * tq + (e & 1);
-                if (mm < M) p.acc_out[((int64_t)mm * p.N + n0 + (e >> 1) * 8) * NG + gg] = __float2int_rn(d[e]);
-              }
-            }
+        for (int a = 0; a < 2; a++) {
+          if (sl0 + a >= nslab) continue;
+          const float* d = a == 0 ? d0 : d1;
+          const int64_t n0 = t * TILE_N + (sl0 + a) * SLAB + g;
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const int mm = 2 * tq + (e & 1);
+            const float v = e < 2 ? d[e] : d[e] * 0.0625f;
+            if (mm < M) p.acc_out[((int64_t)mm * p.N + n0 + (e >> 1) * 8) * NG + gg] = __float2int_rn(v);
           }
         }
       }
     }
     __syncwarp();
-    // After a timeout the stage is not released: the producer's own bounded
-    // wait then expires instead of re-arming a barrier that is still pending.
-    if (ok && lane == 0) mbar_arrive(&empty_bar[s]);
+    if (lane == 0) mbar_arrive(&empty_bar[s]);
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 2; a++) {  // rows g + 8 carry a factor 16 (exact power of two)
+    yacc[a][2] *= 0.0625f;
+    yacc[a][3] *= 0.0625f;
   }
 
   // ---- phase 4: split-K reduction.  Partial sums of position (warp, lane) go

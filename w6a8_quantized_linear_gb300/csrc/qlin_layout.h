@@ -47,12 +47,14 @@ QL_HD int64_t unit_bytes(int bits, int64_t R, int64_t W, int64_t G) {
   return R * (W / G) * 4 + R * W * bits / 8;
 }
 // Activation operand block of one unit (shared memory only): per 32-wide k
-// pair, 32 lanes x 16 bytes of bf16 MMA B fragments, padded to B_PAIR bytes so
+// pair, 32 lanes x 16 bytes of fp16 MMA B fragments, padded to B_PAIR bytes so
 // that the quantising threads' stores to consecutive pairs fall in different
-// banks; then 8 floats per group, the group's start value
-// -(128 + offset) * sum q for each row.
+// banks; then 128 bytes per MMA sub-group (min(G, 128) k): for each of its two
+// chains (k-steps A, B), for each lane quad t, the float4 start value
+// (rows g and g + 8 x activation rows 2t, 2t + 1).
 constexpr int B_PAIR = 528;
-QL_HD int64_t bblock_bytes(int64_t W, int64_t G) { return (W / 32) * B_PAIR + (W / G) * 32; }
+QL_HD int64_t sub_group(int64_t G) { return G < 128 ? G : 128; }
+QL_HD int64_t bblock_bytes(int64_t W, int64_t G) { return (W / 32) * B_PAIR + (W / sub_group(G)) * 128; }
 
 struct Geo {
   int bits;

@@ -79,7 +79,8 @@ __global__ void qlin_repack_write_kernel(RepackParams p) {
             for (int e = 0; e < 2; e++) {
               const int64_t r = slab * 16 + g + 8 * (reg & 1);
               const int64_t k = kbase + 16 * step + 2 * tq + 8 * (reg >> 1) + e;
-              out |= (staged_code<BITS>(tc, row_bytes, r, k) >> 4) << (8 * step + 16 * e + 2 * reg);
+              out |= (staged_code<BITS>(tc, row_bytes, r, k) >> 4)
+                     << (8 * step + 16 * e + 2 * (reg >> 1) + 4 * (reg & 1));
             }
       }
     }
