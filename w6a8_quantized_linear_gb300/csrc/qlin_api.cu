@@ -285,6 +285,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int64_t N, int64_t K, int64_t
   p.red_off = pl.red_off;
   p.stages = pl.stages;
   p.fault_unit = fault_unit;
+  p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
   (void)debug;
   void* args[] = {&p};
   return launch(forward_fn(g.bits, kind, G), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),

@@ -46,7 +46,6 @@
 
 namespace qlin {
 
-constexpr uint32_t F16X2_1024 = 0x64006400u;  // fp16 1024.0 in both halves
 constexpr float RINT_MAGIC = 12582912.0f;     // 1.5 * 2^23: x + M - M rounds x to an integer, ties to even
 
 struct FwdParams {
@@ -67,6 +66,10 @@ struct FwdParams {
   int64_t b_off, red_off;     // dynamic shared memory carve (bytes)
   int stages;
   int64_t fault_unit;         // test only: unit of CTA (0,0) whose copy is never issued (-1: none)
+  // fp16 1024.0 in both halves (0x64006400).  Passed as a parameter, not a
+  // literal, so it lives in a register: each A register is then one
+  // AND-OR instruction with the mask as its immediate.
+  uint32_t f16_base;
 };
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -142,12 +145,12 @@ struct ActSlice {
 // 4-bit plane word; h01 / h23 are the 2-bit plane word shifted so that the top
 // bits of registers 0/1 (2/3) sit at bits 4..5 (row g) and 8..9 (row g + 8).
 template <int BITS>
-__device__ __forceinline__ void unpack_step(uint32_t w, uint32_t h01, uint32_t h23, uint32_t (&a)[4]) {
+__device__ __forceinline__ void unpack_step(uint32_t w, uint32_t h01, uint32_t h23, uint32_t base, uint32_t (&a)[4]) {
   const uint32_t w8 = w >> 8;
-  a[0] = (w & 0x000F000Fu) | F16X2_1024;   // row g:     1024 + c
-  a[1] = (w & 0x00F000F0u) | F16X2_1024;   // row g + 8: 1024 + 16 c
-  a[2] = (w8 & 0x000F000Fu) | F16X2_1024;
-  a[3] = (w8 & 0x00F000F0u) | F16X2_1024;
+  a[0] = (w & 0x000F000Fu) | base;   // row g:     1024 + c
+  a[1] = (w & 0x00F000F0u) | base;   // row g + 8: 1024 + 16 c
+  a[2] = (w8 & 0x000F000Fu) | base;
+  a[3] = (w8 & 0x00F000F0u) | base;
   if (BITS == 6) {
     a[0] |= h01 & 0x00300030u;
     a[1] |= h01 & 0x03000300u;
@@ -160,7 +163,7 @@ __device__ __forceinline__ void unpack_step(uint32_t w, uint32_t h01, uint32_t h
 // The first pair of a sub-group starts each chain at its start value.
 template <int BITS>
 __device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uint4& bq, bool first, const float4& sA,
-                                          const float4& sB, float (&ca)[4], float (&cb)[4]) {
+                                          const float4& sB, uint32_t base, float (&ca)[4], float (&cb)[4]) {
   const uint2 w = *reinterpret_cast<const uint2*>(cp + lane * 8);
   uint32_t hA01 = 0, hA23 = 0, hB01 = 0, hB23 = 0;
   if (BITS == 6) {
@@ -171,8 +174,8 @@ __device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uin
     hB23 = h >> 6;
   }
   uint32_t a[4], b[4];
-  unpack_step<BITS>(w.x, hA01, hA23, a);
-  unpack_step<BITS>(w.y, hB01, hB23, b);
+  unpack_step<BITS>(w.x, hA01, hA23, base, a);
+  unpack_step<BITS>(w.y, hB01, hB23, base, b);
   if (first) {
     mma_f16_16816_c(ca, a[0], a[1], a[2], a[3], bq.x, bq.y, sA.x, sA.y, sA.z, sA.w);
     mma_f16_16816_c(cb, b[0], b[1], b[2], b[3], bq.z, bq.w, sB.x, sB.y, sB.z, sB.w);
@@ -442,7 +445,17 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   const int nslab = R / SLAB;
   const int sl0 = 2 * (warp & 3);
   const int W_last = (int)(p.K - (p.J - 1) * KB);
+  const int64_t i_last = p.J - 1 - j0;  // local index of the row's last unit (may be narrower)
+  // byte offsets inside a unit: the warp's first slab's codes (full / last
+  // unit) and its scales
+  const int cfull = R * GPU * 4 + sl0 * (KB / PAIR_K) * PB, sfull = (KB / PAIR_K) * PB;
+  const int clast = R * (W_last / G) * 4 + sl0 * (W_last / PAIR_K) * PB, slast = (W_last / PAIR_K) * PB;
+  const int ng_last = W_last / G;
+  const int soff0 = (sl0 * 16 + 2 * g) * 4, sgrp = nslab * 64;  // scale byte offsets: slab sl0, per group
+  const uint32_t base = p.f16_base;
   const uint8_t* tile_base = smem + tsel * p.unit_full;
+  const uint8_t* unit = tile_base;
+  const uint8_t* bblk = bop;
   float yacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   int s = 0;
   uint32_t ph = 0;
@@ -454,17 +467,14 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       if (lane == 0) atomicExch(p.status, 4u);
       break;
     }
-    const int W = (j0 + i == p.J - 1) ? W_last : KB;
-    const int ng = W / G;
-    const int slab_bytes = (W / PAIR_K) * PB;
-    const uint8_t* unit = tile_base + (int64_t)s * p.stage_bytes;
-    const float* scl = reinterpret_cast<const float*>(unit);
-    const uint8_t* c0p = unit + R * ng * 4 + sl0 * slab_bytes;
+    const bool last = i == i_last;
+    const int ng = last ? ng_last : GPU;
+    const int slab_bytes = last ? slast : sfull;
+    const uint8_t* c0p = unit + (last ? clast : cfull);
     const uint8_t* c1p = c0p + slab_bytes;
-    const uint8_t* bblk = bop + (int64_t)i * p.bbf;
 #pragma unroll
     for (int gi = 0; gi < GPU; gi++) {
-      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+      float d0[4], d1[4];
 #pragma unroll
       for (int h = 0; h < SPG; h++) {
         const int sg = gi * SPG + h;
@@ -475,17 +485,17 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         for (int pp = 0; pp < PPS; pp++) {
           const int pr = sg * PPS + pp;
           const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * B_PAIR + lane * 16);
-          slab_pair<BITS>(c0p + pr * PB, lane, bq, pp == 0, sA, sB, a0, b0);
-          slab_pair<BITS>(c1p + pr * PB, lane, bq, pp == 0, sA, sB, a1, b1);
+          slab_pair<BITS>(c0p + pr * PB, lane, bq, pp == 0, sA, sB, base, a0, b0);
+          slab_pair<BITS>(c1p + pr * PB, lane, bq, pp == 0, sA, sB, base, a1, b1);
         }
 #pragma unroll
         for (int e = 0; e < 4; e++) {  // exact: integer sums below 2^24
-          d0[e] += a0[e] + b0[e];
-          d1[e] += a1[e] + b1[e];
+          d0[e] = h == 0 ? a0[e] + b0[e] : d0[e] + (a0[e] + b0[e]);
+          d1[e] = h == 0 ? a1[e] + b1[e] : d1[e] + (a1[e] + b1[e]);
         }
       }
-      float2 sw0 = *reinterpret_cast<const float2*>(scl + (gi * nslab + sl0) * 16 + 2 * g);
-      float2 sw1 = *reinterpret_cast<const float2*>(scl + (gi * nslab + sl0 + 1) * 16 + 2 * g);
+      float2 sw0 = *reinterpret_cast<const float2*>(unit + soff0 + gi * sgrp);
+      float2 sw1 = *reinterpret_cast<const float2*>(unit + soff0 + gi * sgrp + 64);
       if (GPU > 1 && gi >= ng) sw0 = sw1 = make_float2(0.f, 0.f);  // group past a narrower unit
       yacc[0][0] = __fmaf_rn(sw0.x, d0[0], yacc[0][0]);
       yacc[0][1] = __fmaf_rn(sw0.x, d0[1], yacc[0][1]);
@@ -513,9 +523,12 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[s]);
+    bblk += p.bbf;
+    unit += p.stage_bytes;
     if (++s == S) {
       s = 0;
       ph ^= 1u;
+      unit = tile_base;
     }
   }
 #pragma unroll
