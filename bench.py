@@ -137,9 +137,38 @@ def max_over_ranks(v: float, ws: int, device) -> float:
     return float(t.item())
 
 
+# ----------------------------------------------------------------------------- ncu traffic
+# DRAM bytes (read + write) per launch of the roofline kernel from an ncu
+# capture, keyed by a hash of the kernel sources it was taken on; a changed
+# kernel reports no traffic until it is captured again.
+KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
+TRAFFIC = {}
+
+
+def kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "w6a8_quantized_linear_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic():
+    return TRAFFIC.get(kernel_hash())
+
+
 # ----------------------------------------------------------------------------- the stack
 class Stack:
-    """Weights, activations and outputs of the 64-layer stack, resident on one GPU."""
+    """Weights, activations and outputs of the 64-layer stack, resident on one GPU.
+
+    Per layer, q/k/v read one RMSNorm input (one gamma), gate/up another, o
+    its own input and down the SwiGLU pair.  A grouped step runs q/k/v and
+    gate/up as multi-weight launches (4 launches per layer); a separate step
+    runs the 7 linears one launch each, on the same inputs."""
+
+    GROUPS = (("qkv", "rmsnorm", ("q", "k", "v")), ("o", "none", ("o",)), ("gate_up", "rmsnorm", ("gate", "up")),
+              ("down", "swiglu", ("down",)))
 
     def __init__(self, device, layers: int, seed: int = 0):
         import torch
@@ -148,46 +177,50 @@ class Stack:
         self.dev = device
         self.layers = layers
         self.G = inputs.STACK_G
-        self.spec = inputs.STACK_LAYER
+        self.shape = {name: (K, N) for name, _, K, N in inputs.STACK_LAYER}
         g = torch.Generator(device=device)
         g.manual_seed(seed)
         lo, hi = inputs.STACK_SCALES
         # weights: checkpoint layout drawn on the GPU, then repacked in place
-        self.weights = []
-        rw_bytes = max(qlin.repack_workspace_bytes("w4a8", N, K, self.G)[1] for _, _, K, N in self.spec)
+        rw_bytes = max(qlin.repack_workspace_bytes("w4a8", N, K, self.G)[1] for K, N in self.shape.values())
         rws = torch.empty(rw_bytes, dtype=torch.uint8, device=device)
-        for l in range(layers):
-            row = []
-            for name, kind, K, N in self.spec:
+        self.weights = []
+        for _ in range(layers):
+            row = {}
+            for name, (K, N) in self.shape.items():
                 ncb = N * K // 2
                 buf = torch.empty(ncb + N * (K // self.G) * 4, dtype=torch.uint8, device=device)
                 buf[:ncb] = torch.randint(0, 256, (ncb,), generator=g, dtype=torch.uint8, device=device)
                 buf[ncb:].view(torch.float32).uniform_(lo, hi, generator=g)
                 qlin.repack(buf, "w4a8", N, K, self.G, ws=rws)
-                row.append(buf)
+                row[name] = buf
             self.weights.append(row)
         del rws
-        self.weight_bytes = sum(b.numel() for row in self.weights for b in row)
+        self.weight_bytes = sum(b.numel() for row in self.weights for b in row.values())
         # activations and outputs: one flat buffer each, laid out compactly for
         # the M of the step (so the end-to-end run moves exactly what a step
         # uses with one transfer each way); sized for M = 8
-        self.act_per_row = sum((2 * K if kind == "swiglu" else K) for _, kind, K, _ in self.spec) * layers
-        self.out_per_row = sum(N for _, _, _, N in self.spec) * layers
+        self.group_k = {"qkv": self.shape["q"][0], "o": self.shape["o"][0], "gate_up": self.shape["gate"][0],
+                        "down": self.shape["down"][0]}
+        self.act_per_row = layers * sum((2 if kind == "swiglu" else 1) * self.group_k[gname]
+                                        for gname, kind, _ in self.GROUPS)
+        self.out_per_row = layers * sum(N for _, N in self.shape.values())
         self.act = torch.randn(8 * self.act_per_row, generator=g, device=device).to(torch.bfloat16)
-        self.gammas = [torch.empty(K, device=device).uniform_(0.5, 1.5, generator=g)
-                       for _ in range(layers) for (_, kind, K, _) in self.spec if kind == "rmsnorm"]
+        self.gammas = [{gname: torch.empty(self.group_k[gname], device=device).uniform_(0.5, 1.5, generator=g)
+                        for gname, kind, _ in self.GROUPS if kind == "rmsnorm"} for _ in range(layers)]
         self.out = torch.zeros(8 * self.out_per_row, dtype=torch.float32, device=device)
-        nbytes = max(qlin.forward_workspace_bytes("w4a8", N, K, self.G) for _, _, K, N in self.spec)
+        nbytes = max(qlin.forward_workspace_bytes("w4a8", N, K, self.G) for K, N in self.shape.values())
         self.ws = qlin.new_workspace(nbytes, device)
         torch.cuda.synchronize(device)
 
-    def calls(self, M: int):
-        """(kind, N, K, packed, x, gate, up, gamma, y) of every call of one step at M rows."""
-        a_off = o_off = gi = 0
+    def groups(self, M: int):
+        """(group name, prologue, [names], K, [N], [packed], x, gate, up, gamma, [y]) per launch group of a step."""
+        a_off = o_off = 0
         out = []
         for l in range(self.layers):
-            for (name, kind, K, N), w in zip(self.spec, self.weights[l]):
-                x = gate = up = gamma = None
+            for gname, kind, names in self.GROUPS:
+                K = self.group_k[gname]
+                x = gate = up = None
                 if kind == "swiglu":
                     gate = self.act[a_off:a_off + M * K].view(M, K)
                     up = self.act[a_off + M * K:a_off + 2 * M * K].view(M, K)
@@ -195,49 +228,43 @@ class Stack:
                 else:
                     x = self.act[a_off:a_off + M * K].view(M, K)
                     a_off += M * K
-                if kind == "rmsnorm":
-                    gamma = self.gammas[gi]
-                    gi += 1
-                y = self.out[o_off:o_off + M * N].view(M, N)
-                o_off += M * N
-                out.append((kind, N, K, w, x, gate, up, gamma, y))
+                gamma = self.gammas[l].get(gname)
+                Ns, ys = [], []
+                for n in names:
+                    N = self.shape[n][1]
+                    Ns.append(N)
+                    ys.append(self.out[o_off:o_off + M * N].view(M, N))
+                    o_off += M * N
+                out.append((gname, kind, names, K, Ns, [self.weights[l][n] for n in names], x, gate, up, gamma, ys))
         return out
 
-    def step_graph(self, M: int, stream):
-        import torch
-
+    def launch(self, grp, stream, grouped: bool):
         from w6a8_quantized_linear_gb300 import qlin
-        calls = self.calls(M)
-        # warm the plans outside capture
-        for kind, N, K, w, x, gate, up, gamma, y in calls[:7]:
+        gname, kind, names, K, Ns, ws_, x, gate, up, gamma, ys = grp
+        if grouped and len(names) > 1:
+            qlin.forward_multi("w4a8", kind, ws_, Ns, K, self.G, x=x, gate=gate, up=up, gamma=gamma, y=ys,
+                               ws=self.ws, flags=qlin.FLAG_PDL, stream=stream)
+            return 1
+        for N, w, y in zip(Ns, ws_, ys):
             qlin.forward("w4a8", kind, w, N, K, self.G, x=x, gate=gate, up=up, gamma=gamma, y=y, ws=self.ws,
                          flags=qlin.FLAG_PDL, stream=stream)
+        return len(names)
+
+    def graph(self, M: int, stream, grouped: bool = True, only: str | None = None):
+        """One CUDA graph of a step (or of one launch group across all layers)."""
+        import torch
+        grps = [g for g in self.groups(M) if only is None or g[0] == only]
+        for grp in grps[:4]:  # plans are made outside capture
+            self.launch(grp, stream, grouped)
         torch.cuda.synchronize(self.dev)
         g = torch.cuda.CUDAGraph()
+        n = 0
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
-                for kind, N, K, w, x, gate, up, gamma, y in calls:
-                    qlin.forward("w4a8", kind, w, N, K, self.G, x=x, gate=gate, up=up, gamma=gamma, y=y,
-                                 ws=self.ws, flags=qlin.FLAG_PDL, stream=stream)
-        return g, len(calls)
-
-    def shape_graphs(self, M: int, stream):
-        """One graph per linear type, running that linear for every layer."""
-        import torch
-
-        from w6a8_quantized_linear_gb300 import qlin
-        calls = self.calls(M)
-        out = {}
-        for i, (name, kind, K, N) in enumerate(self.spec):
-            sel = calls[i::len(self.spec)]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                with torch.cuda.graph(g, stream=stream):
-                    for kind_, N_, K_, w, x, gate, up, gamma, y in sel:
-                        qlin.forward("w4a8", kind_, w, N_, K_, self.G, x=x, gate=gate, up=up, gamma=gamma, y=y,
-                                     ws=self.ws, flags=qlin.FLAG_PDL, stream=stream)
-            out[name] = (g, len(sel), sum(w.numel() for (_, _, _, w, *_r) in sel))
-        return out
+                for grp in grps:
+                    n += self.launch(grp, stream, grouped)
+        nbytes = sum(w.numel() for grp in grps for w in grp[5])
+        return g, n, nbytes
 
 
 def time_graph(g, stream, iters: int, warmup: int, ws_world=1, device=None):
@@ -314,28 +341,35 @@ def run_reference(args):
 
 
 def run_linear(args):
-    """C calls of one linear type of the stack (distinct weights), for profilers."""
+    """C launches of one linear of the stack, or of one launch group (qkv,
+    gate_up: multi-weight), on distinct weights, once; for profilers."""
     import torch
 
     import __graft_entry__
     __graft_entry__.build()
     from w6a8_quantized_linear_gb300 import inputs, qlin
     spec = {name: (kind, K, N) for name, kind, K, N in inputs.STACK_LAYER}
-    kind, K, N = spec[args.linear]
+    groups = {"qkv": ("q", "k", "v"), "gate_up": ("gate", "up")}
+    names = groups.get(args.linear, (args.linear,))
+    kind, K, _ = spec[names[0]]
+    Ns = [spec[n][2] for n in names]
     G = inputs.STACK_G
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     lo, hi = inputs.STACK_SCALES
-    ws = qlin.new_workspace(qlin.forward_workspace_bytes("w4a8", N, K, G), dev)
+    ws = qlin.new_workspace(qlin.forward_workspace_bytes("w4a8", max(Ns), K, G), dev)
     calls = []
     for _ in range(args.calls):
-        ncb = N * K // 2
-        w = torch.empty(qlin.packed_bytes("w4a8", N, K, G), dtype=torch.uint8, device=dev)
-        w[:ncb] = torch.randint(0, 256, (ncb,), generator=g, dtype=torch.uint8, device=dev)
-        w[ncb:].view(torch.float32).uniform_(lo, hi, generator=g)
-        qlin.repack(w, "w4a8", N, K, G)
+        ws_ = []
+        for N in Ns:
+            ncb = N * K // 2
+            w = torch.empty(qlin.packed_bytes("w4a8", N, K, G), dtype=torch.uint8, device=dev)
+            w[:ncb] = torch.randint(0, 256, (ncb,), generator=g, dtype=torch.uint8, device=dev)
+            w[ncb:].view(torch.float32).uniform_(lo, hi, generator=g)
+            qlin.repack(w, "w4a8", N, K, G)
+            ws_.append(w)
         x = gate = up = gamma = None
         if kind == "swiglu":
             gate = torch.randn(args.M, K, generator=g, device=dev).to(torch.bfloat16)
@@ -344,13 +378,14 @@ def run_linear(args):
             x = torch.randn(args.M, K, generator=g, device=dev).to(torch.bfloat16)
         if kind == "rmsnorm":
             gamma = torch.empty(K, device=dev).uniform_(0.5, 1.5, generator=g)
-        calls.append((w, x, gate, up, gamma, torch.empty(args.M, N, device=dev)))
-    for w, x, gate, up, gamma, y in calls:
-        qlin.forward("w4a8", kind, w, N, K, G, x=x, gate=gate, up=up, gamma=gamma, y=y, ws=ws, flags=qlin.FLAG_PDL)
+        calls.append((ws_, x, gate, up, gamma, [torch.empty(args.M, N, device=dev) for N in Ns]))
+    for ws_, x, gate, up, gamma, ys in calls:
+        qlin.forward_multi("w4a8", kind, ws_, Ns, K, G, x=x, gate=gate, up=up, gamma=gamma, y=ys, ws=ws,
+                           flags=qlin.FLAG_PDL)
     torch.cuda.synchronize()
     assert qlin.read_device_status(ws) == qlin.OK
-    print(json.dumps({"linear": args.linear, "M": args.M, "N": N, "K": K, "calls": args.calls,
-                      "launch": qlin.launch_info("w4a8", N, K, G)}))
+    print(json.dumps({"linear": args.linear, "M": args.M, "N": Ns, "K": K, "calls": args.calls,
+                      "bytes_per_launch": sum(qlin.packed_bytes("w4a8", N, K, G) for N in Ns)}))
     return 0
 
 
@@ -366,11 +401,15 @@ def main():
     ap.add_argument("--linear", default=None, help="profile mode: one linear type of the stack")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--print-kernel-hash", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.linear is not None:
         return run_linear(args)
+    if args.print_kernel_hash:
+        print(kernel_hash())
+        return 0
     if args.warmup < 3:
         args.warmup = 3
 
@@ -387,9 +426,10 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     peak, peak_kind = load_peaks()
 
-    g1, ncalls = stack.step_graph(1, stream)
-    g8, _ = stack.step_graph(8, stream)
-    kernels_per_step = ncalls
+    g1, ncalls, wb = stack.graph(1, stream)
+    g8, _, _ = stack.graph(8, stream)
+    s1, ncalls_sep, _ = stack.graph(1, stream, grouped=False)
+    s8, _, _ = stack.graph(8, stream, grouped=False)
 
     with ClockSampler(local) as clk:
         t1 = time_graph(g1, stream, args.steps, args.warmup, world, dev)
@@ -397,18 +437,22 @@ def main():
     clocks = clk.summary()
     t1 = max_over_ranks(t1, world, dev)
     t8 = max_over_ranks(t8, world, dev)
-    wb = stack.weight_bytes
     gbs1 = world * wb / (t1 * 1e-3) / 1e9
     gbs8 = world * wb / (t8 * 1e-3) / 1e9
+    ts1 = time_graph(s1, stream, max(3, args.steps // 2), 3)
+    ts8 = time_graph(s8, stream, max(3, args.steps // 2), 3)
 
-    # per linear type (64 launches each, graph replay): where the time goes
+    # per launch group (64 launches each, graph replay): where the time goes
     per = {}
-    for name, (g, n, nbytes) in stack.shape_graphs(1, stream).items():
-        t = time_graph(g, stream, max(3, args.steps // 2), 2)
-        per[name] = {"us_per_call": t * 1e3 / n, "GB/s": nbytes / (t * 1e-3) / 1e9}
-    for name, (g, n, nbytes) in stack.shape_graphs(8, stream).items():
-        t = time_graph(g, stream, max(3, args.steps // 2), 2)
-        per[name]["us_per_call_m8"] = t * 1e3 / n
+    for gname, _, _ in Stack.GROUPS:
+        for M in (1, 8):
+            g, n, nbytes = stack.graph(M, stream, only=gname)
+            t = time_graph(g, stream, max(3, args.steps // 2), 3)
+            e = per.setdefault(gname, {"launches_per_step": n})
+            e[f"us_per_launch_m{M}"] = t * 1e3 / n
+            e[f"GB/s_m{M}"] = nbytes / (t * 1e-3) / 1e9
+            e["bytes_per_launch"] = nbytes // n
+            del g
 
     # end to end through the public call with host buffers: pinned host
     # activations in, every call's output back, each step
@@ -445,29 +489,39 @@ def main():
                "sample": "one layer of the stack (q,k,v,o,gate,up,down) at M=1, 181,043,200 weight bytes, "
                          f"{dt:.1f} s"}
 
-    # algorithmic bytes per call: packed weight + activation operand read + y written
-    alg_bytes = wb + 2 * stack.act_per_row + 4 * stack.out_per_row  # weights + M=1 activations + outputs
-    achieved = alg_bytes / (t1 * 1e-3) / 1e9
+    # roofline of the dominant launch (gate/up: two 17408x5120 weights on one
+    # RMSNorm input), timed live above with CUDA events on the launching
+    # stream: algorithmic bytes = both packed weights + x + gamma + both y
+    Kg, Ng = stack.shape["gate"]
+    gu_bytes = 2 * qlin.packed_bytes("w4a8", Ng, Kg, stack.G) + 2 * Kg + 4 * Kg + 2 * 4 * Ng
+    gu_us = per["gate_up"]["us_per_launch_m1"]
+    achieved = gu_bytes / (gu_us * 1e-6) / 1e9
+    traffic = kernel_traffic()
     line = {
         "metric": METRIC, "value": gbs1, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t1, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "w4a8 (int8 x int4 codes, exact on bf16 MMA, fp32 accumulate)",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 1, "layers": args.layers, "calls_per_step": ncalls,
+        "vs_baseline": None, "dtype": "w4a8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "layers": args.layers, "launches_per_step": ncalls,
+                   "grouping": "q/k/v and gate/up as multi-weight launches sharing one prologue; o, down alone",
                    "weight_bytes_per_step": wb, "l2": "inputs larger than L2 (weights streamed once per step)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": 100.0 * gbs1 / world / peak, "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
         "pct_of_8tbs_spec": 100.0 * gbs1 / world / 8000.0,
         "m8": {"value": gbs8, "ms_per_step": t8, "pct_of_hbm_peak": 100.0 * gbs8 / world / peak},
         "t8_over_t1": t8 / t1,
-        "per_linear": per,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "kernel": "qlin_forward (prologue + GEMV, PDL-overlapped), average over the step's calls"},
+        "separate_launches": {"launches_per_step": ncalls_sep, "value": world * wb / (ts1 * 1e-3) / 1e9,
+                              "ms_per_step": ts1, "m8": world * wb / (ts8 * 1e-3) / 1e9, "t8_over_t1": ts8 / ts1},
+        "per_group": per,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic["bytes_per_launch"] if traffic else None,
+                     "kernel": "qlin_forward_kernel<4,1,128>: the gate/up multi-weight launch, M=1, "
+                               f"{gu_bytes} algorithmic bytes per launch, {gu_us:.2f} us per launch (CUDA events, "
+                               "64 launches in a graph)",
+                     "traffic_source": traffic["source"] if traffic else "kernel changed since the last ncu capture"},
         "cpu_baseline": cpu,
         "e2e": {"value": gbs_e2e, "unit": "GB/s", "ms_per_step": te2e,
                 "h2d_bytes_per_step": h_act.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 4},
-        "gpu_launches": kernels_per_step * args.steps,
+        "gpu_launches": ncalls * args.steps,
         "clocks": clocks,
     }
     if rank == 0:

@@ -173,6 +173,33 @@ qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int
                          const float* gamma, float eps, float* y,
                          void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
+/*
+ * Several weights that read the same activation, in one launch [LIN], [ACT]:
+ * y[l] = packed[l] x quantised activation for l = 0..n-1, e.g. the q, k and v
+ * projections after one RMSNorm, or gate and up.  The prologue and the
+ * activation quantisation are computed for the shared input only; fusing the
+ * steps that share an input follows "Doubling the LLM token rate in
+ * ComfyUI", section "Optimising the linear kernel" (the prologue is absorbed
+ * into the quantisation and the launches between them disappear).
+ *   n             : 1..QLIN_MAX_MULTI weights.
+ *   N             : host array [n] of output rows (each N[l] obeys the rules
+ *                   of qlin_forward; N[l] = 0 skips weight l).
+ *   packed        : host array [n] of device pointers, each a repacked stream
+ *                   of shape (N[l], K, G), 16-byte aligned.
+ *   y             : host array [n] of device pointers, fp32 [M, N[l]]
+ *                   row-major, 4-byte aligned; fully overwritten.
+ *   All other arguments, the numerics and the errors are those of
+ *   qlin_forward; the host arrays are read during the call only.  Each y[l]
+ *   equals qlin_forward on weight l within the output tolerance; the
+ *   split-K order may differ because the cluster size is chosen for the
+ *   whole launch.
+ */
+#define QLIN_MAX_MULTI 8
+qlin_status qlin_forward_multi(int fmt, int prologue, int M, int n, const int64_t* N, int64_t K, int64_t G,
+                               const void* const* packed, const void* x, const void* gate, const void* up,
+                               const float* gamma, float eps, float* const* y, void* ws, size_t ws_bytes,
+                               unsigned flags, void* stream);
+
 /* Launch shape of qlin_forward's GEMV on the current device: CTAs, stream
  * units (128 rows x KB columns) and bytes of `packed` read per call. */
 qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G,

@@ -129,3 +129,31 @@ def test_repack_rejects_bad_arguments(L):
 def test_debug_fault_rejects_negative_unit(L):
     assert L.qlin_debug_forward_fault(0, 0, 1, 512, 256, 32, 256, 256, None, None, None, 1e-6, 256, 256, 1 << 20,
                                       -1, None) == qlin.ERR_INVALID_ARG
+
+
+def test_forward_multi_rejects_bad_arguments(L):
+    import ctypes
+
+    def call(n=2, Ns=(512, 256), packed=(256, 512), ys=(256, 512), K=256, G=32, x=256, ws=256, flags=0):
+        na = (ctypes.c_int64 * max(1, len(Ns)))(*Ns) if Ns is not None else None
+        pa = (ctypes.c_void_p * max(1, len(packed)))(*packed) if packed is not None else None
+        ya = (ctypes.c_void_p * max(1, len(ys)))(*ys) if ys is not None else None
+        return L.qlin_forward_multi(0, 0, 1, n, ctypes.cast(na, ctypes.c_void_p) if na else None, K, G,
+                                    ctypes.cast(pa, ctypes.c_void_p) if pa else None, x, None, None, None, 1e-6,
+                                    ctypes.cast(ya, ctypes.c_void_p) if ya else None, ws, 1 << 20, flags, None)
+
+    assert call(n=0) == qlin.ERR_INVALID_ARG
+    assert call(n=9, Ns=(16,) * 9, packed=(256,) * 9, ys=(256,) * 9) == qlin.ERR_INVALID_ARG
+    assert call(Ns=None) == qlin.ERR_INVALID_ARG
+    assert call(packed=None) == qlin.ERR_INVALID_ARG
+    assert call(ys=None) == qlin.ERR_INVALID_ARG
+    assert call(Ns=(512, 24)) == qlin.ERR_UNSUPPORTED           # one weight's N % 16
+    assert call(Ns=(512, -16)) == qlin.ERR_INVALID_ARG
+    assert call(packed=(256, 8)) == qlin.ERR_INVALID_ARG        # misaligned second weight
+    assert call(ys=(256, 0)) == qlin.ERR_INVALID_ARG            # missing second output
+    assert call(ys=(256, 2)) == qlin.ERR_INVALID_ARG            # misaligned second output
+    assert call(x=264) == qlin.ERR_INVALID_ARG
+    assert call(flags=4) == qlin.ERR_INVALID_ARG
+    assert call(Ns=(0, 0)) == qlin.OK                           # nothing to do
+    assert call(Ns=(0, 256), packed=(0, 512), ys=(0, 512), ws=None) == qlin.ERR_INVALID_ARG
+

@@ -146,8 +146,7 @@ int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
 // clusters the device holds at once give the waves of the launch; the cost is
 // waves x stream units of the busiest CTA.  The cheapest C wins, ties going
 // to the smaller cluster.  Caller holds g_mu.
-qlin_status make_plan(const Geo& g, DevCache& dc, int kind, Plan* out) {
-  const int64_t NB = (g.T + TILES_PER_CTA - 1) / TILES_PER_CTA;
+qlin_status make_plan(const Geo& g, int64_t NB, DevCache& dc, int kind, Plan* out) {
   const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
   const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
   const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
@@ -227,55 +226,76 @@ qlin_status check_act(int kind, int M, const void* x, const void* gate, const vo
   return QLIN_OK;
 }
 
-struct Outputs {
-  float* y = nullptr;
+// 256-row blocks of a weight with N output rows
+int64_t row_blocks(int64_t N) { return ((N + TILE_N - 1) / TILE_N + TILES_PER_CTA - 1) / TILES_PER_CTA; }
+
+struct Outputs {  // test exports of a single-weight call
   int32_t* acc = nullptr;
   int8_t* q = nullptr;
   float* s = nullptr;
 };
 
-qlin_status forward_impl(int fmt, int kind, int M, int64_t N, int64_t K, int64_t G, const void* packed,
-                         const void* x, const void* gate, const void* up, const float* gamma, float eps,
-                         const Outputs& out, void* ws, size_t ws_bytes, unsigned flags, void* stream, bool debug,
-                         int64_t fault_unit = -1) {
-  qlin_status st = check_shape_impl(fmt, N, K, G);
-  if (st != QLIN_OK) return st;
+// One launch over n weights that share the format, K, G and the activation
+// input: argument checks, the plan, the parameter block, the launch.
+qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int64_t K, int64_t G,
+                         const void* const* packed, const void* x, const void* gate, const void* up,
+                         const float* gamma, float eps, float* const* ys, const Outputs& out, void* ws,
+                         size_t ws_bytes, unsigned flags, void* stream, bool debug, int64_t fault_unit = -1) {
+  if (n < 1 || n > MAX_LIN || !Ns || !packed || !ys) return QLIN_ERR_INVALID_ARG;
+  qlin_status st = QLIN_OK;
+  int64_t NB = 0;
+  for (int l = 0; l < n; l++) {
+    st = check_shape_impl(fmt, Ns[l], K, G);
+    if (st != QLIN_OK) return st;
+    NB += row_blocks(Ns[l]);
+  }
   st = check_act(kind, M, x, gate, up, gamma, eps);
   if (st != QLIN_OK) return st;
   if (flags & ~QLIN_FLAG_PDL) return QLIN_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return QLIN_OK;
-  if (!packed || !aligned(packed, 16)) return QLIN_ERR_INVALID_ARG;
-  if (!debug && !out.y) return QLIN_ERR_INVALID_ARG;
-  if ((out.y && !aligned(out.y, 4)) || (out.acc && !aligned(out.acc, 4)) || (out.s && !aligned(out.s, 4)))
-    return QLIN_ERR_INVALID_ARG;
+  if (M == 0 || NB == 0) return QLIN_OK;
+  for (int l = 0; l < n; l++) {
+    if (Ns[l] == 0) continue;
+    if (!packed[l] || !aligned(packed[l], 16)) return QLIN_ERR_INVALID_ARG;
+    if (!debug && !ys[l]) return QLIN_ERR_INVALID_ARG;
+    if (ys[l] && !aligned(ys[l], 4)) return QLIN_ERR_INVALID_ARG;
+  }
+  if ((out.acc && !aligned(out.acc, 4)) || (out.s && !aligned(out.s, 4))) return QLIN_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return QLIN_ERR_INVALID_ARG;
   if (ws_bytes < (size_t)WS_HEADER) return QLIN_ERR_WORKSPACE;
-  const Geo g = make_geo(fmt, N, K, G);
+  const Geo g = make_geo(fmt, 0, K, G);  // the K geometry every weight shares
   Plan pl;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, *dc, kind, &pl);
+    st = make_plan(g, NB, *dc, kind, &pl);
     if (st != QLIN_OK) return st;
   }
   FwdParams p;
-  p.packed = static_cast<const uint8_t*>(packed);
+  std::memset(&p, 0, sizeof(p));
+  int nl = 0;
+  for (int l = 0; l < n; l++) {  // weights with no rows take no block
+    if (Ns[l] == 0) continue;
+    p.packed[nl] = static_cast<const uint8_t*>(packed[l]);
+    p.y[nl] = ys[l];
+    p.N[nl] = Ns[l];
+    p.T[nl] = (Ns[l] + TILE_N - 1) / TILE_N;
+    p.blk0[nl + 1] = p.blk0[nl] + row_blocks(Ns[l]);
+    nl++;
+  }
+  p.n_lin = nl;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.gate = static_cast<const __nv_bfloat16*>(gate);
   p.up = static_cast<const __nv_bfloat16*>(up);
   p.gamma = gamma;
   p.eps = eps;
-  p.y = out.y;
   p.status = static_cast<uint32_t*>(ws);
   p.acc_out = out.acc;
   p.q_out = out.q;
   p.s_out = out.s;
   p.M = M;
-  p.N = N;
   p.K = K;
-  p.T = g.T;
   p.J = g.J;
   p.tile_full = g.tile_full;
   p.unit_full = g.unit_full;
@@ -286,7 +306,6 @@ qlin_status forward_impl(int fmt, int kind, int M, int64_t N, int64_t K, int64_t
   p.stages = pl.stages;
   p.fault_unit = fault_unit;
   p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
-  (void)debug;
   void* args[] = {&p};
   return launch(forward_fn(g.bits, kind, G), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
                 dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args, pl.C,
@@ -436,10 +455,16 @@ qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G, const void* packed,
                          const void* x, const void* gate, const void* up, const float* gamma, float eps, float* y,
                          void* ws, size_t ws_bytes, unsigned flags, void* stream) {
-  Outputs o;
-  o.y = y;
-  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, o, ws, ws_bytes, flags, stream,
-                      false);
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, Outputs(), ws, ws_bytes,
+                      flags, stream, false);
+}
+
+qlin_status qlin_forward_multi(int fmt, int prologue, int M, int n, const int64_t* N, int64_t K, int64_t G,
+                               const void* const* packed, const void* x, const void* gate, const void* up,
+                               const float* gamma, float eps, float* const* y, void* ws, size_t ws_bytes,
+                               unsigned flags, void* stream) {
+  return forward_impl(fmt, prologue, M, n, N, K, G, packed, x, gate, up, gamma, eps, y, Outputs(), ws, ws_bytes,
+                      flags, stream, false);
 }
 
 qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, int64_t* ctas, int64_t* units,
@@ -454,7 +479,7 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, i
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, *dc, QLIN_PROLOGUE_NONE, &pl);
+    st = make_plan(g, row_blocks(N), *dc, QLIN_PROLOGUE_NONE, &pl);
     if (st != QLIN_OK) return st;
   }
   *ctas = (int64_t)pl.C * pl.NB;
@@ -477,11 +502,11 @@ qlin_status qlin_debug_forward(int fmt, int prologue, int M, int64_t N, int64_t 
                                float* y, int32_t* acc, int8_t* q, float* s, void* ws, size_t ws_bytes,
                                void* stream) {
   Outputs o;
-  o.y = y;
   o.acc = acc;
   o.q = q;
   o.s = s;
-  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, o, ws, ws_bytes, 0, stream, true);
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, o, ws, ws_bytes, 0, stream,
+                      true);
 }
 
 qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
@@ -489,10 +514,8 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
                                      const float* gamma, float eps, float* y, void* ws, size_t ws_bytes,
                                      int64_t unit, void* stream) {
   if (unit < 0) return QLIN_ERR_INVALID_ARG;
-  Outputs o;
-  o.y = y;
-  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, o, ws, ws_bytes, 0, stream, false,
-                      unit);
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, Outputs(), ws, ws_bytes, 0,
+                      stream, false, unit);
 }
 
 qlin_status qlin_forward_noalloc(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
@@ -507,10 +530,8 @@ qlin_status qlin_forward_noalloc(int fmt, int prologue, int M, int64_t N, int64_
   void* ws = nullptr;
   st = noalloc_scratch(&ws);
   if (st != QLIN_OK) return st;
-  Outputs o;
-  o.y = y;
-  return forward_impl(fmt, prologue, M, N, K, G, packed, x, gate, up, gamma, eps, o, ws, NOALLOC_SCRATCH_BYTES, flags,
-                      stream, false);
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, Outputs(), ws,
+                      NOALLOC_SCRATCH_BYTES, flags, stream, false);
 }
 
 }  // extern "C"

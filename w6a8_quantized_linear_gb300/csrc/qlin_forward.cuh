@@ -49,19 +49,25 @@ namespace qlin {
 constexpr float RINT_MAGIC = 12582912.0f;     // 1.5 * 2^23: x + M - M rounds x to an integer, ties to even
 
 struct FwdParams {
-  const uint8_t* packed;
+  // The weights of one launch: n_lin weights that share K, G, the format and
+  // the activation input; their 256-row blocks run end to end along
+  // blockIdx.y (weight l owns blocks [blk0[l], blk0[l + 1])).
+  int n_lin;
+  const uint8_t* packed[MAX_LIN];
+  float* y[MAX_LIN];          // [M, N[l]]
+  int64_t N[MAX_LIN], T[MAX_LIN];
+  int64_t blk0[MAX_LIN + 1];
   const __nv_bfloat16* x;     // NONE, RMSNORM: [M, K]
   const __nv_bfloat16* gate;  // SWIGLU: [M, K]
   const __nv_bfloat16* up;    // SWIGLU: [M, K]
   const float* gamma;         // RMSNORM: [K]
   float eps;
-  float* y;                   // [M, N]
   uint32_t* status;           // workspace status word
-  int32_t* acc_out;           // test export: [M, N, K/G] exact group sums
+  int32_t* acc_out;           // test export (single weight): [M, N, K/G] exact group sums
   int8_t* q_out;              // test export: [M, K] activation codes
   float* s_out;               // test export: [M] row scales
   int M;
-  int64_t N, K, T, J;
+  int64_t K, J;
   int64_t tile_full, unit_full, bbf, stage_bytes;
   int64_t b_off, red_off;     // dynamic shared memory carve (bytes)
   int stages;
@@ -215,12 +221,27 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   }
   const uint32_t crank = cluster_ctarank();
   const int C = (int)gridDim.x;
-  const int64_t rb = blockIdx.y;
+  // this CTA's weight (constant indices only: the parameter block is never
+  // indexed at run time)
+  const uint8_t* packed = p.packed[0];
+  float* y = p.y[0];
+  int64_t N = p.N[0], T = p.T[0], blk_first = 0;
+#pragma unroll
+  for (int l = 1; l < MAX_LIN; l++) {
+    if (l < p.n_lin && (int64_t)blockIdx.y >= p.blk0[l]) {
+      packed = p.packed[l];
+      y = p.y[l];
+      N = p.N[l];
+      T = p.T[l];
+      blk_first = p.blk0[l];
+    }
+  }
+  const int64_t rb = (int64_t)blockIdx.y - blk_first;
   const int64_t j0 = split_begin(crank, p.J, C), j1 = split_begin(crank + 1, p.J, C);
   const int nu = (int)(j1 - j0);
   const int64_t k_lo = j0 * KB, k_hi = min(p.K, j1 * KB), n8 = (k_hi - k_lo) / 8;
   const int64_t tA = rb * TILES_PER_CTA;
-  const bool hasB = tA + 1 < p.T;
+  const bool hasB = tA + 1 < T;
   const int S = p.stages;
   const int M = p.M;
   // split-K positions (consumer thread slots) this CTA owns and finishes
@@ -247,9 +268,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      const int64_t RA = min((int64_t)TILE_N, p.N - tA * TILE_N);
-      const int64_t RB = hasB ? min((int64_t)TILE_N, p.N - (tA + 1) * TILE_N) : 0;
-      const uint8_t* srcA = p.packed + tA * p.tile_full;
+      const int64_t RA = min((int64_t)TILE_N, N - tA * TILE_N);
+      const int64_t RB = hasB ? min((int64_t)TILE_N, N - (tA + 1) * TILE_N) : 0;
+      const uint8_t* srcA = packed + tA * p.tile_full;
       const uint8_t* srcB = srcA + p.tile_full;
       const int64_t strideA = unit_bytes(BITS, RA, KB, G), strideB = unit_bytes(BITS, RB, KB, G);
       const bool fault_cta = blockIdx.x == 0 && blockIdx.y == 0;
@@ -351,7 +372,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     s_row[tid][0] = s;
     s_row[tid][1] = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
     s_row[tid][2] = rs;
-    if (p.s_out && rb == 0 && crank == 0) p.s_out[tid] = s;
+    if (p.s_out && blockIdx.y == 0 && crank == 0) p.s_out[tid] = s;
   }
   consumer_bar();
 
@@ -396,7 +417,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
               qf[e] = q;
               rowsum[m] += q;
             }
-            if (p.q_out && rb == 0) {
+            if (p.q_out && blockIdx.y == 0) {
 #pragma unroll
               for (int e = 0; e < 8; e++) p.q_out[(int64_t)m * p.K + k_lo + kl + e] = (int8_t)(int)qf[e];
             }
@@ -441,7 +462,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   const int g = lane >> 2, tq = lane & 3;
   const int tsel = warp >> 2;  // which of the CTA's two tiles this warp works on
   const int64_t t = tA + tsel;
-  const int R = (tsel == 0 || hasB) ? (int)min((int64_t)TILE_N, p.N - t * TILE_N) : 0;
+  const int R = (tsel == 0 || hasB) ? (int)min((int64_t)TILE_N, N - t * TILE_N) : 0;
   const int nslab = R / SLAB;
   const int sl0 = 2 * (warp & 3);
   const int W_last = (int)(p.K - (p.J - 1) * KB);
@@ -516,7 +537,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
           for (int e = 0; e < 4; e++) {
             const int mm = 2 * tq + (e & 1);
             const float v = e < 2 ? d[e] : d[e] * 0.0625f;
-            if (mm < M) p.acc_out[((int64_t)mm * p.N + n0 + (e >> 1) * 8) * NG + gg] = __float2int_rn(v);
+            if (mm < M) p.acc_out[((int64_t)mm * N + n0 + (e >> 1) * 8) * NG + gg] = __float2int_rn(v);
           }
         }
       }
@@ -549,7 +570,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     st_async_f4(dst, make_float4(yacc[0][0], yacc[0][1], yacc[0][2], yacc[0][3]), rbar);
     st_async_f4(dst + 16, make_float4(yacc[1][0], yacc[1][1], yacc[1][2], yacc[1][3]), rbar);
     if (!mbar_wait_cluster(&red_bar, 0) && lane == 0) atomicExch(p.status, 4u);
-    if (tid < pos1 - pos0 && p.y != nullptr) {
+    if (tid < pos1 - pos0 && y != nullptr) {
       const int pos = pos0 + tid;
       float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int r = 0; r < C; r++) {  // fixed rank order
@@ -560,7 +581,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       }
       const int w_src = pos >> 5, l_src = pos & 31, gs = l_src >> 2, ts = l_src & 3;
       const int64_t tt = tA + (w_src >> 2);
-      const int64_t Rt = (w_src < 4 || hasB) ? min((int64_t)TILE_N, p.N - tt * TILE_N) : 0;
+      const int64_t Rt = (w_src < 4 || hasB) ? min((int64_t)TILE_N, N - tt * TILE_N) : 0;
       const float sm0 = 2 * ts < M ? s_row[2 * ts][0] : 0.f;
       const float sm1 = 2 * ts + 1 < M ? s_row[2 * ts + 1][0] : 0.f;
 #pragma unroll
@@ -569,12 +590,12 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         if (slab * SLAB >= Rt) continue;
         const int64_t n = tt * TILE_N + slab * SLAB + gs;
         if (2 * ts < M) {
-          p.y[(int64_t)(2 * ts) * p.N + n] = sm0 * v[4 * a + 0];
-          p.y[(int64_t)(2 * ts) * p.N + n + 8] = sm0 * v[4 * a + 2];
+          y[(int64_t)(2 * ts) * N + n] = sm0 * v[4 * a + 0];
+          y[(int64_t)(2 * ts) * N + n + 8] = sm0 * v[4 * a + 2];
         }
         if (2 * ts + 1 < M) {
-          p.y[(int64_t)(2 * ts + 1) * p.N + n] = sm1 * v[4 * a + 1];
-          p.y[(int64_t)(2 * ts + 1) * p.N + n + 8] = sm1 * v[4 * a + 3];
+          y[(int64_t)(2 * ts + 1) * N + n] = sm1 * v[4 * a + 1];
+          y[(int64_t)(2 * ts + 1) * N + n + 8] = sm1 * v[4 * a + 3];
         }
       }
     }

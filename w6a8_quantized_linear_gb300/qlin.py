@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
                 "qlin_workspace_init": (st, [vp, sz, vp]),
                 "qlin_forward": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz,
                                       ctypes.c_uint, vp]),
+                "qlin_forward_multi": (st, [i32, i32, i32, i32, vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float,
+                                            vp, vp, sz, ctypes.c_uint, vp]),
                 "qlin_forward_launch_info": (st, [i32, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                                   ctypes.POINTER(i64)]),
                 "qlin_read_device_status": (st, [vp, vp]),
@@ -164,6 +166,34 @@ def forward(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, x=None,
     _check(lib().qlin_forward(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate), _ptr(up),
                               _ptr(gamma), float(eps), _ptr(y), _ptr(ws), ws.numel(), flags, _stream(stream)),
            "forward")
+    return y
+
+
+MAX_MULTI = 8
+
+
+def forward_multi(fmt, prologue, packed: list, N: list, K: int, G: int, x=None, gate=None, up=None, gamma=None,
+                  eps: float = 1e-6, y: list | None = None, ws: torch.Tensor | None = None, flags: int = 0,
+                  stream=None) -> list:
+    """Several weights on one shared activation in one launch: y[l] = packed[l] x
+    quantised prologue(activation).  Returns the list of fp32 [M, N[l]] outputs."""
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    n = len(packed)
+    if len(N) != n:
+        raise ValueError("packed and N differ in length")
+    dev = packed[0].device
+    if y is None:
+        y = [torch.empty(M, Nl, dtype=torch.float32, device=dev) for Nl in N]
+    if ws is None:
+        ws = new_workspace(forward_workspace_bytes(fmt, max(N), K, G), dev, stream)
+    n_arr = (ctypes.c_int64 * n)(*N)
+    p_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in packed])
+    y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in y])
+    _check(lib().qlin_forward_multi(_fmt(fmt), _pro(prologue), M, n, ctypes.cast(n_arr, ctypes.c_void_p), K, G,
+                                    ctypes.cast(p_arr, ctypes.c_void_p), _ptr(x), _ptr(gate), _ptr(up), _ptr(gamma),
+                                    float(eps), ctypes.cast(y_arr, ctypes.c_void_p), _ptr(ws), ws.numel(), flags,
+                                    _stream(stream)), "forward_multi")
     return y
 
 
