@@ -73,12 +73,13 @@ typedef enum {
 } qlin_prologue;
 
 /* qlin_forward flags. */
-#define QLIN_FLAG_PDL 1u /* Launch with programmatic dependent launch: the GEMV may start
-                            streaming `packed` while earlier kernels in `stream` still run.
-                            The caller asserts that `packed` was not written by any kernel
-                            still in flight in `stream` (true for model weights repacked
-                            at load time).  Activations, gamma, y and the workspace are
-                            still touched only after earlier kernels complete. */
+#define QLIN_FLAG_PDL 1u /* Launch with programmatic dependent launch: the kernel may start
+                            streaming `packed` and reading `gamma` while earlier kernels in
+                            `stream` still run.  The caller asserts that neither was written
+                            by any kernel still in flight in `stream` (true for model
+                            weights repacked at load time and for norm weights).
+                            Activations, y and the workspace are still touched only after
+                            earlier kernels complete. */
 
 /* Library version string. */
 const char* qlin_version(void);
@@ -160,7 +161,8 @@ qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * Numerics: the prologue and the scale s_m = amax/127 are computed in fp32,
  * q = clamp(round-half-even(a / s_m), -127, 127) (s_m = 0, q = 0 for an
  * all-zero row; with no prologue a / s_m is the IEEE fp32 quotient, with a
- * prologue a * (127 / amax)); group sums are exact integers; y is accumulated
+ * prologue a * c, c = rstd * 127 / amax from fast fp32 reciprocals, which the
+ * method's tolerance allows); group sums are exact integers; y is accumulated
  * in fp32 in a fixed order that depends on (N, K, G) and the device, never on
  * M or on the other rows, so row m of an 8-row call equals the same row run
  * alone.  One kernel is enqueued: a cluster of CTAs per 256 output rows

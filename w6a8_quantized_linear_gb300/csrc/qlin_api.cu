@@ -98,9 +98,9 @@ struct Plan {
 
 // Shared-memory carve: [stages][activation operand][split-K slots].  Fails
 // when the budget holds fewer than min_stages stages (or the CTA's units).
-bool carve(const Geo& g, Plan& pl, int64_t budget, int64_t min_stages) {
+bool carve(const Geo& g, int64_t bbf, Plan& pl, int64_t budget, int64_t min_stages) {
   pl.stage_bytes = round_up(2 * g.unit_full, 128);
-  const int64_t b_bytes = round_up(pl.upc * g.bbf, 128);
+  const int64_t b_bytes = round_up(pl.upc * bbf, 128);
   const int64_t cmax = (CONSUMERS + pl.C - 1) / pl.C;
   const int64_t red_bytes = round_up((int64_t)pl.C * cmax * 8 * 4, 128);
   const int64_t rest = b_bytes + red_bytes + 128;
@@ -146,7 +146,7 @@ int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
 // clusters the device holds at once give the waves of the launch; the cost is
 // waves x stream units of the busiest CTA.  The cheapest C wins, ties going
 // to the smaller cluster.  Caller holds g_mu.
-qlin_status make_plan(const Geo& g, int64_t NB, DevCache& dc, int kind, Plan* out) {
+qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int kind, Plan* out) {
   const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
   const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
   const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
@@ -159,7 +159,7 @@ qlin_status make_plan(const Geo& g, int64_t NB, DevCache& dc, int kind, Plan* ou
     pl.NB = NB;
     pl.C = (int)c;
     pl.upc = (int)((g.J + c - 1) / c);
-    if (!(carve(g, pl, SMEM_TWO_PER_SM, 3) || carve(g, pl, SMEM_MAX, 2))) continue;
+    if (!(carve(g, bbf, pl, SMEM_TWO_PER_SM, 3) || carve(g, bbf, pl, SMEM_MAX, 2))) continue;
     const int n = active_clusters(dc, fn, pl.C, pl.smem);
     if (n < 1) continue;
     const int64_t cost = (NB + n - 1) / n * pl.upc;
@@ -269,7 +269,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, NB, *dc, kind, &pl);
+    st = make_plan(g, NB, bblock_bytes(g.KB, G, M), *dc, kind, &pl);
     if (st != QLIN_OK) return st;
   }
   FwdParams p;
@@ -296,10 +296,12 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
   p.s_out = out.s;
   p.M = M;
   p.K = K;
+  p.inv_k = 1.0f / (float)K;
   p.J = g.J;
   p.tile_full = g.tile_full;
   p.unit_full = g.unit_full;
-  p.bbf = g.bbf;
+  p.bpm = (int)bpair_bytes(M);
+  p.bbf = (int)bblock_bytes(g.KB, G, M);
   p.stage_bytes = pl.stage_bytes;
   p.b_off = pl.b_off;
   p.red_off = pl.red_off;
@@ -479,7 +481,7 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, i
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, row_blocks(N), *dc, QLIN_PROLOGUE_NONE, &pl);
+    st = make_plan(g, row_blocks(N), bblock_bytes(g.KB, G, MAX_M), *dc, QLIN_PROLOGUE_NONE, &pl);
     if (st != QLIN_OK) return st;
   }
   *ctas = (int64_t)pl.C * pl.NB;

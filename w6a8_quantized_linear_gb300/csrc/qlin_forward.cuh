@@ -68,7 +68,9 @@ struct FwdParams {
   float* s_out;               // test export: [M] row scales
   int M;
   int64_t K, J;
-  int64_t tile_full, unit_full, bbf, stage_bytes;
+  float inv_k;                // 1 / K (RMSNorm mean)
+  int64_t tile_full, unit_full, stage_bytes;
+  int bpm, bbf;               // activation operand: bytes per 32-wide pair, per unit block
   int64_t b_off, red_off;     // dynamic shared memory carve (bytes)
   int stages;
   int64_t fault_unit;         // test only: unit of CTA (0,0) whose copy is never issued (-1: none)
@@ -97,50 +99,74 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 r, float (&v)[8]) {
   }
 }
 
-// The activation slice of one thread: 8 consecutive k of every row (and the
-// matching gamma).  All loads are issued before any is used.  Activations are
-// read through L2 (the previous kernel in the stream may have written them).
+// The activation slice of one thread: 8 consecutive k of every row.  All
+// loads are issued before any is used.  Activations are read through L2 (the
+// previous kernel in the stream may have written them); gamma, a parameter of
+// the model like the weights, is loaded separately (possibly before that
+// kernel completes, under QLIN_FLAG_PDL).  SwiGLU values are computed once, at
+// load, and kept in fp32.
 template <int KIND>
 struct ActSlice {
-  uint4 a[MAX_M];                     // x (NONE, RMSNORM) or gate (SWIGLU)
-  uint4 b[KIND == 2 ? MAX_M : 1];     // up (SWIGLU)
+  uint4 a[KIND == 2 ? 1 : MAX_M];     // x (NONE, RMSNORM)
+  float v[KIND == 2 ? MAX_M : 1][8];  // silu(gate) * up (SWIGLU)
   float4 g0, g1;                      // gamma (RMSNORM)
 
-  __device__ __forceinline__ void load(const FwdParams& p, int M, int64_t k) {
-#pragma unroll
-    for (int m = 0; m < MAX_M; m++) {
-      if (m < M) {
-        if (KIND == 2) {
-          a[m] = __ldcg(reinterpret_cast<const uint4*>(p.gate + (int64_t)m * p.K + k));
-          b[m] = __ldcg(reinterpret_cast<const uint4*>(p.up + (int64_t)m * p.K + k));
-        } else {
-          a[m] = __ldcg(reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + k));
-        }
-      }
-    }
+  __device__ __forceinline__ void load_gamma(const FwdParams& p, int64_t k) {
     if (KIND == 1) {
       g0 = __ldcg(reinterpret_cast<const float4*>(p.gamma + k));
       g1 = __ldcg(reinterpret_cast<const float4*>(p.gamma + k + 4));
     }
   }
-  // Prologue value before the row scale: none a = x; RMSNorm t = x * gamma
-  // (rstd comes later) and ss += x^2; SwiGLU a = g * u / (1 + e^-g).
-  __device__ __forceinline__ void value(int m, float (&v)[8], float& ss) const {
+  __device__ __forceinline__ void load(const FwdParams& p, int M, int64_t k) {
     if (KIND == 2) {
-      float g[8], u[8];
-      bf16x8_to_f32(a[m], g);
-      bf16x8_to_f32(b[KIND == 2 ? m : 0], u);
+      // the raw bf16 words land in the registers of v (gate in 0..3, up in
+      // 4..7) and each row is converted in place, so raw and converted rows
+      // never need separate registers
 #pragma unroll
-      for (int e = 0; e < 8; e++)
-        v[e] = __fmul_rn(__fmul_rn(g[e], u[e]), __frcp_rn(__fadd_rn(1.0f, __expf(-g[e]))));
+      for (int m = 0; m < MAX_M; m++) {
+        if (m < M) {
+          const uint4 gq = __ldcg(reinterpret_cast<const uint4*>(p.gate + (int64_t)m * p.K + k));
+          const uint4 uq = __ldcg(reinterpret_cast<const uint4*>(p.up + (int64_t)m * p.K + k));
+          v[m][0] = __uint_as_float(gq.x); v[m][1] = __uint_as_float(gq.y);
+          v[m][2] = __uint_as_float(gq.z); v[m][3] = __uint_as_float(gq.w);
+          v[m][4] = __uint_as_float(uq.x); v[m][5] = __uint_as_float(uq.y);
+          v[m][6] = __uint_as_float(uq.z); v[m][7] = __uint_as_float(uq.w);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < MAX_M; m++) {
+        if (m < M) {
+          const uint4 gq = make_uint4(__float_as_uint(v[m][0]), __float_as_uint(v[m][1]), __float_as_uint(v[m][2]),
+                                      __float_as_uint(v[m][3]));
+          const uint4 uq = make_uint4(__float_as_uint(v[m][4]), __float_as_uint(v[m][5]), __float_as_uint(v[m][6]),
+                                      __float_as_uint(v[m][7]));
+          float g[8], u[8];
+          bf16x8_to_f32(gq, g);
+          bf16x8_to_f32(uq, u);
+#pragma unroll
+          for (int e = 0; e < 8; e++) v[m][e] = __fdividef(__fmul_rn(g[e], u[e]), __fadd_rn(1.0f, __expf(-g[e])));
+        }
+      }
     } else {
-      bf16x8_to_f32(a[m], v);
+#pragma unroll
+      for (int m = 0; m < MAX_M; m++)
+        if (m < M) a[m] = __ldcg(reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + k));
+    }
+  }
+  // Prologue value before the row factor: none a = x; RMSNorm t = x * gamma
+  // (rstd comes later) and ss += x^2; SwiGLU a = g * u / (1 + e^-g).
+  __device__ __forceinline__ void value(int m, float (&out)[8], float& ss) const {
+    if (KIND == 2) {
+#pragma unroll
+      for (int e = 0; e < 8; e++) out[e] = v[m][e];
+    } else {
+      bf16x8_to_f32(a[m], out);
       if (KIND == 1) {
         const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
         for (int e = 0; e < 8; e++) {
-          ss = __fmaf_rn(v[e], v[e], ss);
-          v[e] = __fmul_rn(v[e], gm[e]);
+          ss = __fmaf_rn(out[e], out[e], ss);
+          out[e] = __fmul_rn(out[e], gm[e]);
         }
       }
     }
@@ -200,7 +226,6 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   constexpr int PPS = SG / PAIR_K;       // 32-wide pairs per sub-group
   constexpr int SEG = SG / 8;            // lanes whose 8 k make one sub-group (quantisation pass)
   constexpr int PB = BITS == 6 ? 384 : 256;
-  constexpr int CIN = (KB / PAIR_K) * B_PAIR;  // start values after the fragments of a block
 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
@@ -209,7 +234,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   __shared__ __align__(8) uint64_t red_bar;   // completes when every rank's partial sums have landed
   __shared__ float s_red[CONSUMER_WARPS][MAX_M][2];
   __shared__ __align__(16) float s_slot[MAX_CLUSTER][MAX_M][2];  // rank r's (amax, sum x^2) per row
-  __shared__ float s_row[MAX_M][3];                               // s, 127 / amax, rstd
+  __shared__ float s_row[MAX_M][2];                               // s, code factor c
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // TMA destinations and vector loads need 16-byte alignment of the dynamic
@@ -244,6 +269,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   const bool hasB = tA + 1 < T;
   const int S = p.stages;
   const int M = p.M;
+  const int BPM = p.bpm, CIN = (KB / PAIR_K) * BPM;  // operand pair stride; start values follow the pairs
   // split-K positions (consumer thread slots) this CTA owns and finishes
   const int pos0 = (int)(crank * CONSUMERS / C), pos1 = (int)((crank + 1) * CONSUMERS / C);
 
@@ -308,12 +334,13 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   }
 
   // -------------------------------------------------------------------- consumers
-  pdl_wait();  // activations may be written by the previous kernel in the stream
   uint8_t* bop = smem + p.b_off;  // activation operand blocks, one per unit of this CTA
   const int rounds = (int)((n8 + CONSUMERS - 1) / CONSUMERS);
+  ActSlice<KIND> act;
+  if (tid < n8) act.load_gamma(p, k_lo + tid * 8);  // a model parameter: may be read early
+  pdl_wait();  // activations may be written by the previous kernel in the stream
 
   // ---- phase 1: prologue statistics of this CTA's K range, per row
-  ActSlice<KIND> act;
   {
     float amax[MAX_M], ssq[MAX_M];
 #pragma unroll
@@ -321,6 +348,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     for (int r = 0; r < rounds; r++) {
       const int64_t i8 = (int64_t)r * CONSUMERS + tid;
       if (i8 < n8) {
+        if (r > 0) act.load_gamma(p, k_lo + i8 * 8);
         act.load(p, M, k_lo + i8 * 8);
 #pragma unroll
         for (int m = 0; m < MAX_M; m++) {
@@ -363,15 +391,22 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       a = fmaxf(a, s_slot[r][tid][0]);
       q = __fadd_rn(q, s_slot[r][tid][1]);
     }
-    float rs = 1.0f, amax = a;
-    if (KIND == 1) {
-      rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(q, (float)p.K), p.eps)));
-      amax = __fmul_rn(a, rs);  // = max |fl(x*gamma) * rstd| (rounding is monotone)
+    // Row scale s and the factor c that maps a prologue value to its code
+    // (a * c = a / s).  With no prologue s and the quotients are IEEE, so the
+    // codes equal the definition bit for bit; with a prologue the tolerance
+    // of the method allows the fast reciprocal forms.
+    float s, c;
+    if (KIND == 0) {
+      s = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+      c = 0.f;
+    } else {
+      const float rs = KIND == 1 ? rsqrtf(__fadd_rn(__fmul_rn(q, p.inv_k), p.eps)) : 1.0f;
+      const float amax = __fmul_rn(a, rs);  // = max |fl(x*gamma) * rstd| (rounding is monotone)
+      s = amax * (1.0f / 127.0f);
+      c = amax > 0.f ? __fmul_rn(rs, __fdividef(127.0f, amax)) : 0.f;
     }
-    const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
     s_row[tid][0] = s;
-    s_row[tid][1] = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-    s_row[tid][2] = rs;
+    s_row[tid][1] = c;
     if (p.s_out && blockIdx.y == 0 && crank == 0) p.s_out[tid] = s;
   }
   consumer_bar();
@@ -388,7 +423,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     for (int r = 0; r < rounds2; r++) {
       const int64_t i8 = (int64_t)r * CONSUMERS + tid;
       const bool inb = i8 < n8f, valid = i8 < n8;
-      if (valid && rounds > 1) act.load(p, M, k_lo + i8 * 8);
+      if (valid && rounds > 1) {
+        act.load_gamma(p, k_lo + i8 * 8);
+        act.load(p, M, k_lo + i8 * 8);
+      }
       const int64_t kl = i8 * 8, jl = kl / KB;
       const int kin = (int)(kl - jl * KB);
       uint8_t* blk = bop + jl * p.bbf;
@@ -402,18 +440,18 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
           if (valid) {
             float v[8], ss = 0.f;
             act.value(m, v, ss);
-            const float s = s_row[m][0], mul = s_row[m][1], rs = s_row[m][2];
+            const float s = s_row[m][0], c = s_row[m][1];
+            // |t| <= 127 (1 + a few ulp) because |a| <= amax, so round half to
+            // even never leaves [-127, 127]: no clamp is needed
 #pragma unroll
             for (int e = 0; e < 8; e++) {
               float t;
               if (KIND == 0) {
                 t = s > 0.f ? __fdiv_rn(v[e], s) : 0.f;  // IEEE division: codes identical to the definition
               } else {
-                const float a = KIND == 1 ? __fmul_rn(v[e], rs) : v[e];
-                t = __fmul_rn(a, mul);
+                t = __fmul_rn(v[e], c);
               }
-              float q = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);  // round half to even
-              q = fminf(fmaxf(q, -127.0f), 127.0f);
+              const float q = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);  // round half to even
               qf[e] = q;
               rowsum[m] += q;
             }
@@ -428,7 +466,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
 #pragma unroll
           for (int t = 0; t < 4; t++) {
             const __half2 h2 = __floats2half2_rn(qf[2 * t], qf[2 * t + 1]);  // exact: |q| <= 127
-            *reinterpret_cast<__half2*>(blk + pr * B_PAIR + (4 * m + t) * 16 + step * 8 + half * 4) = h2;
+            *reinterpret_cast<__half2*>(blk + pr * BPM + (4 * m + t) * 16 + step * 8 + half * 4) = h2;
           }
         }
       }
@@ -436,9 +474,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       // is the k-step, so summing over the other bits gives each chain's sum
 #pragma unroll
       for (int m = 0; m < MAX_M; m++) {
+        if (m < M) {  // M is the same in every lane
 #pragma unroll
-        for (int o = 1; o < SEG; o <<= 1)
-          if (o != 2) rowsum[m] += __shfl_xor_sync(0xffffffffu, rowsum[m], o);
+          for (int o = 1; o < SEG; o <<= 1)
+            if (o != 2) rowsum[m] += __shfl_xor_sync(0xffffffffu, rowsum[m], o);
+        }
       }
       if (inb && (lane % SEG) < 4 && (lane & 1) == 0) {
         const int chain = (lane >> 1) & 1;
@@ -474,6 +514,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   const int ng_last = W_last / G;
   const int soff0 = (sl0 * 16 + 2 * g) * 4, sgrp = nslab * 64;  // scale byte offsets: slab sl0, per group
   const uint32_t base = p.f16_base;
+  const int blane = (g < M ? lane : tq) * 16;  // rows M..7 read row 0's fragments (their columns are dropped)
   const uint8_t* tile_base = smem + tsel * p.unit_full;
   const uint8_t* unit = tile_base;
   const uint8_t* bblk = bop;
@@ -505,7 +546,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
 #pragma unroll
         for (int pp = 0; pp < PPS; pp++) {
           const int pr = sg * PPS + pp;
-          const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * B_PAIR + lane * 16);
+          const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * BPM + blane);
           slab_pair<BITS>(c0p + pr * PB, lane, bq, pp == 0, sA, sB, base, a0, b0);
           slab_pair<BITS>(c1p + pr * PB, lane, bq, pp == 0, sA, sB, base, a1, b1);
         }

@@ -48,14 +48,19 @@ QL_HD int64_t unit_bytes(int bits, int64_t R, int64_t W, int64_t G) {
   return R * (W / G) * 4 + R * W * bits / 8;
 }
 // Activation operand block of one unit (shared memory only): per 32-wide k
-// pair, 32 lanes x 16 bytes of fp16 MMA B fragments, padded to B_PAIR bytes so
-// that the quantising threads' stores to consecutive pairs fall in different
-// banks; then 128 bytes per MMA sub-group (min(G, 128) k): for each of its two
-// chains (k-steps A, B), for each lane quad t, the float4 start value
-// (rows g and g + 8 x activation rows 2t, 2t + 1).
-constexpr int B_PAIR = 528;
+// pair, the fp16 MMA B fragments of the lanes that hold real activation rows
+// (lanes 0 .. 4M-1, 16 bytes each), padded by 16 bytes so that the quantising
+// threads' stores to consecutive pairs fall in different banks; then 128 bytes
+// per MMA sub-group (min(G, 128) k): for each of its two chains (k-steps A,
+// B), for each lane quad t, the float4 start value (rows g and g + 8 x
+// activation rows 2t, 2t + 1).  Lanes of rows M..7 read row 0's fragments:
+// an MMA column depends on its own B column only, and those columns are never
+// written out.
+QL_HD int64_t bpair_bytes(int64_t M) { return 64 * M + 16; }
 QL_HD int64_t sub_group(int64_t G) { return G < 128 ? G : 128; }
-QL_HD int64_t bblock_bytes(int64_t W, int64_t G) { return (W / 32) * B_PAIR + (W / sub_group(G)) * 128; }
+QL_HD int64_t bblock_bytes(int64_t W, int64_t G, int64_t M) {
+  return (W / 32) * bpair_bytes(M) + (W / sub_group(G)) * 128;
+}
 
 struct Geo {
   int bits;
@@ -64,7 +69,6 @@ struct Geo {
   int64_t J;        // units per tile
   int64_t U;        // units
   int64_t tile_full;   // bytes of a 128-row tile
-  int64_t bbf;         // bytes of a full activation block (stride)
   int64_t unit_full;   // bytes of a full 128-row unit
 };
 
@@ -77,7 +81,6 @@ QL_HD Geo make_geo(int fmt, int64_t N, int64_t K, int64_t G) {
   g.J = (K + g.KB - 1) / g.KB;
   g.U = g.T * g.J;
   g.tile_full = unit_bytes(g.bits, TILE_N, K, G);
-  g.bbf = bblock_bytes(g.KB, G);
   g.unit_full = unit_bytes(g.bits, TILE_N, g.KB, G);
   return g;
 }
