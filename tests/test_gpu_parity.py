@@ -87,6 +87,48 @@ def test_activation_codes(kind, M, K, G):
         assert np.allclose(sh, ref["s"], rtol=2e-6, atol=0)
 
 
+def _near_tie_rows(n_rows: int, K: int) -> np.ndarray:
+    """Rows whose quotients x / s sit on or next to a rounding boundary, where
+    a product with the rounded reciprocal of s rounds differently from the IEEE
+    quotient (found by enumerating bf16 values; s = fl32(amax / 127))."""
+    grid = (np.arange(0x3C00, 0x43C8, dtype=np.uint32) << 16).view(np.float32)
+    rows = []
+    for abits in range(0x4280, 0x43C0):
+        amax = np.array([abits << 16], dtype=np.uint32).view(np.float32)[0]
+        s = np.float32(amax / np.float32(127))
+        x = grid[grid <= amax]
+        q = (x / s).astype(np.float32)
+        t = (x * np.float32(np.float32(1) / s)).astype(np.float32)
+        hit = x[np.rint(t) != np.rint(q)]
+        if hit.size:
+            row = np.zeros(K, np.float32)
+            v = np.concatenate([[amax], hit[:60], -hit[:60]])[:K]
+            row[:v.size] = v
+            rows.append(row)
+        if len(rows) == n_rows:
+            break
+    assert len(rows) == n_rows
+    return np.stack(rows)
+
+
+def test_no_prologue_codes_exact_near_ties():
+    """With no prologue the codes are rne(fl(x / s)) bit for bit, also where
+    the kernel's fast product with fl(1 / s) lands on the other side of a
+    rounding boundary than the IEEE quotient."""
+    K = 256
+    x = _near_tie_rows(8, K)
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    assert torch.equal(xt.float(), torch.from_numpy(x))  # all exact in bf16
+    c = inputs.make_case("w4a8", "none", 8, 16, K, 32, seed=5)
+    c.x = xt
+    d = device_case(c)
+    r = qlin.debug_forward("w4a8", "none", d["w"], 16, K, 32, x=d["x"])
+    ref = oracle_forward(c)
+    assert np.array_equal(r["q"].cpu().numpy().astype(np.int64), ref["q"])
+    assert np.array_equal(r["s"].cpu().numpy().astype(np.float64), ref["s"])
+    assert np.array_equal(r["acc"].cpu().numpy().astype(np.int64), ref["acc"])
+
+
 # ---------------------------------------------------------------- exact group sums
 @pytest.mark.parametrize("fmt", ["w4a8", "w6a8"])
 @pytest.mark.parametrize("kind", ["none", "rmsnorm", "swiglu"])
