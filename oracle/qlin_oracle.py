@@ -14,6 +14,7 @@ step in float64 / int64 with numpy:
 3. per-row symmetric int8 quantisation       -- ``quantize_rows``
 4. per-group integer dot products            -- ``group_acc``
 5. y = s_m * sum_g sw[n,g] * acc[m,n,g]      -- ``forward``
+   (+ bias[n] when the layer has a float bias)
 
 plus ``unpack_stream``, an independent reading of the kernel-order stream
 layout that the in-place repack produces (used to check the GPU repack byte
@@ -34,7 +35,9 @@ Sources (page title, section):
   when it has no codebook, ``w6a8_int8`` has none, weights are symmetric;
   shape rules for K and G.
 * same page, section "Activations and smoothing": integer formats take float
-  input and quantise activations inside the kernel, with no stored input scale.
+  input and quantise activations inside the kernel, with no stored input scale;
+  biases stay floating point (section "Checkpoint layout": an ordinary float
+  bias beside the quantised weight, if present).
 
 Readings where the pages are silent (each is listed in the design notes):
 
@@ -241,8 +244,10 @@ def group_acc(q, codes, fmt: str, G: int) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 def forward(fmt: str, kind: str, N: int, K: int, G: int, buf, x=None, gate=None, up=None,
-            gamma=None, eps: float = 1e-6, cols=None, stream: bool = False) -> dict:
-    """y[M, N] = s_m * sum_g sw[n, g] * acc[m, n, g], in float64, rounded to fp32.
+            gamma=None, eps: float = 1e-6, cols=None, stream: bool = False, bias=None) -> dict:
+    """y[M, N] = s_m * sum_g sw[n, g] * acc[m, n, g] (+ bias[n]), in float64,
+    rounded to fp32.  ``bias`` is an optional fp32 [N] vector (reading: an
+    ordinary float bias is added after the scaled product).
 
     ``buf`` is the checkpoint layout (or, with ``stream=True``, the repacked
     stream layout).  ``cols`` restricts the computation to the listed output
@@ -259,6 +264,9 @@ def forward(fmt: str, kind: str, N: int, K: int, G: int, buf, x=None, gate=None,
     q, s, v = quantize_rows(a, fp32=(kind == "none"))
     acc = group_acc(q, codes, fmt, G)
     y64 = s[:, None] * (acc.astype(np.float64) * sw.astype(np.float64)[None, :, :]).sum(axis=2)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float32).astype(np.float64)
+        y64 = y64 + (b if cols is None else b[np.asarray(cols)])[None, :]
     return {"y": y64.astype(np.float32), "y64": y64, "q": q, "s": s, "v": v, "acc": acc, "a": a}
 
 

@@ -115,7 +115,7 @@ def check_file_layout(O, seed=1):
 def check_forward_bruteforce(O, seed=2):
     rng = random.Random(seed)
     for fmt in ("w4a8", "w6a8"):
-        for (N, K, G) in ((16, 32, 32), (16, 64, 32), (32, 128, 64), (16, 128, 32)):
+        for (N, K, G) in ((16, 32, 32), (16, 64, 32), (32, 128, 64), (16, 128, 32), (16, 64, 16), (32, 96, 16)):
             M = rng.randint(1, 8)
             gen = torch.Generator().manual_seed(rng.randint(0, 10**6))
             x = torch.randn(M, K, generator=gen).to(torch.bfloat16)
@@ -123,8 +123,13 @@ def check_forward_bruteforce(O, seed=2):
             codes = torch.randint(0, 256, (nb,), generator=gen, dtype=torch.uint8).numpy()
             sw = torch.empty(N * (K // G)).uniform_(0.01, 0.02, generator=gen).numpy().astype("<f4")
             wbuf = np.concatenate([codes, sw.view(np.uint8)])
-            r = O.forward(fmt, "none", N, K, G, wbuf, x=bits_of(x))
+            bias = None
+            if rng.random() < 0.5:
+                bias = torch.randn(N, generator=gen).numpy().astype(np.float32)
+            r = O.forward(fmt, "none", N, K, G, wbuf, x=bits_of(x), bias=bias)
             yb = _bruteforce_y(fmt, N, K, G, wbuf, r["q"], r["s"])
+            if bias is not None:
+                yb = yb + bias.astype(np.float64)[None, :]
             assert np.allclose(r["y64"], yb, rtol=1e-12, atol=1e-12 * np.abs(yb).max()), (fmt, N, K, G)
 
 
@@ -283,3 +288,26 @@ def check_stream_bijection(O):
             hkey = hsrc * 4 + (slot >> 4)
             assert np.unique(hkey).size == N * K, fmt
             assert not np.intersect1d(src, hsrc).size, "2-bit plane shares bytes with the 4-bit plane"
+
+
+def check_bias(O, seed=9):
+    """A float bias is added once, unscaled, to every row: with every level zero
+    y equals the bias exactly; sampled columns take the matching entries."""
+    rng = np.random.default_rng(seed)
+    for fmt in ("w4a8", "w6a8"):
+        b = {"w4a8": 4, "w6a8": 6}[fmt]
+        N, K, G = 32, 128, 32
+        bias = rng.normal(size=N).astype(np.float32) * 3
+        sw = rng.uniform(0.01, 0.02, (N, K // G)).astype(np.float32)
+        x = torch.randn(3, K, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+        zero = O.pack_file(fmt, np.full((N, K), 1 << (b - 1)), sw)
+        r = O.forward(fmt, "none", N, K, G, zero, x=bits_of(x), bias=bias)
+        assert np.array_equal(r["y"], np.broadcast_to(bias, (3, N))), fmt
+        codes = rng.integers(0, 1 << b, (N, K))
+        wbuf = O.pack_file(fmt, codes, sw)
+        full = O.forward(fmt, "rmsnorm", N, K, G, wbuf, x=bits_of(x), gamma=np.ones(K, np.float32), bias=bias)
+        cols = np.array([0, 5, 17, 31])
+        part = O.forward(fmt, "rmsnorm", N, K, G, wbuf, x=bits_of(x), gamma=np.ones(K, np.float32), bias=bias,
+                         cols=cols)
+        assert np.array_equal(part["y64"], full["y64"][:, cols]), fmt
+
