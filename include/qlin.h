@@ -42,8 +42,8 @@
  *    read back by qlin_read_device_status; the kernel returns instead of
  *    hanging.
  *  - fmt is QLIN_W4A8 or QLIN_W6A8; b = 4 or 6 bits per code.
- *  - Backend limits beyond [OPT] (QLIN_ERR_UNSUPPORTED): G in {32, 64, 128,
- *    256} (so K % 32 == 0), N % 16 == 0, K <= 65536, M <= 8.
+ *  - Backend limits beyond [OPT] (QLIN_ERR_UNSUPPORTED): G in {16, 32, 64,
+ *    128, 256}, K % 32 == 0, N % 16 == 0, K <= 65536, M <= 8.
  */
 #ifndef QLIN_H_
 #define QLIN_H_
@@ -190,6 +190,11 @@ qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int
  *                   of shape (N[l], K, G), 16-byte aligned.
  *   y             : host array [n] of device pointers, fp32 [M, N[l]]
  *                   row-major, 4-byte aligned; fully overwritten.
+ *   bias          : NULL, or a host array [n] of device pointers (each NULL or
+ *                   fp32 [N[l]], 4-byte aligned): y[l][m][n] gets bias[l][n]
+ *                   added once, unscaled ("Comfy Quantization Formats",
+ *                   sections "Checkpoint layout" and "Activations and
+ *                   smoothing": a layer's bias stays floating point).
  *   All other arguments, the numerics and the errors are those of
  *   qlin_forward; the host arrays are read during the call only.  Each y[l]
  *   equals qlin_forward on weight l within the output tolerance; the
@@ -199,8 +204,8 @@ qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int
 #define QLIN_MAX_MULTI 8
 qlin_status qlin_forward_multi(int fmt, int prologue, int M, int n, const int64_t* N, int64_t K, int64_t G,
                                const void* const* packed, const void* x, const void* gate, const void* up,
-                               const float* gamma, float eps, float* const* y, void* ws, size_t ws_bytes,
-                               unsigned flags, void* stream);
+                               const float* gamma, float eps, float* const* y, const float* const* bias, void* ws,
+                               size_t ws_bytes, unsigned flags, void* stream);
 
 /* Launch shape of qlin_forward's GEMV on the current device: CTAs, stream
  * units (128 rows x KB columns) and bytes of `packed` read per call. */

@@ -51,7 +51,10 @@ def test_version_and_status_strings(L):
     ("w4a8", 16, 96, 64, qlin.ERR_INVALID_ARG),    # K % G
     ("w6a8", 16, 48, 16, qlin.ERR_INVALID_ARG),    # K % 32
     ("w6a8", 16, 64, 8, qlin.ERR_INVALID_ARG),     # G % 16
-    ("w4a8", 16, 64, 16, qlin.ERR_UNSUPPORTED),    # legal, below this backend's G range
+    ("w4a8", 16, 64, 16, qlin.OK),                 # one group per 16-wide k-step
+    ("w6a8", 32, 96, 16, qlin.OK),
+    ("w4a8", 16, 48, 16, qlin.ERR_UNSUPPORTED),    # legal, K % 32 != 0 (this backend works in 32-wide pairs)
+    ("w4a8", 16, 64, 8, qlin.ERR_UNSUPPORTED),     # legal, below this backend's G range
     ("w4a8", 16, 64, 4, qlin.ERR_UNSUPPORTED),
     ("w4a8", 16, 1024, 512, qlin.ERR_UNSUPPORTED),
     ("w4a8", 24, 256, 32, qlin.ERR_UNSUPPORTED),   # N % 16
@@ -134,13 +137,15 @@ def test_debug_fault_rejects_negative_unit(L):
 def test_forward_multi_rejects_bad_arguments(L):
     import ctypes
 
-    def call(n=2, Ns=(512, 256), packed=(256, 512), ys=(256, 512), K=256, G=32, x=256, ws=256, flags=0):
+    def call(n=2, Ns=(512, 256), packed=(256, 512), ys=(256, 512), K=256, G=32, x=256, ws=256, flags=0, bias=None):
+        ba = (ctypes.c_void_p * len(bias))(*bias) if bias is not None else None
         na = (ctypes.c_int64 * max(1, len(Ns)))(*Ns) if Ns is not None else None
         pa = (ctypes.c_void_p * max(1, len(packed)))(*packed) if packed is not None else None
         ya = (ctypes.c_void_p * max(1, len(ys)))(*ys) if ys is not None else None
         return L.qlin_forward_multi(0, 0, 1, n, ctypes.cast(na, ctypes.c_void_p) if na else None, K, G,
                                     ctypes.cast(pa, ctypes.c_void_p) if pa else None, x, None, None, None, 1e-6,
-                                    ctypes.cast(ya, ctypes.c_void_p) if ya else None, ws, 1 << 20, flags, None)
+                                    ctypes.cast(ya, ctypes.c_void_p) if ya else None,
+                                    ctypes.cast(ba, ctypes.c_void_p) if ba else None, ws, 1 << 20, flags, None)
 
     assert call(n=0) == qlin.ERR_INVALID_ARG
     assert call(n=9, Ns=(16,) * 9, packed=(256,) * 9, ys=(256,) * 9) == qlin.ERR_INVALID_ARG
@@ -154,6 +159,7 @@ def test_forward_multi_rejects_bad_arguments(L):
     assert call(ys=(256, 2)) == qlin.ERR_INVALID_ARG            # misaligned second output
     assert call(x=264) == qlin.ERR_INVALID_ARG
     assert call(flags=4) == qlin.ERR_INVALID_ARG
+    assert call(bias=(0, 2)) == qlin.ERR_INVALID_ARG            # misaligned bias
     assert call(Ns=(0, 0)) == qlin.OK                           # nothing to do
     assert call(Ns=(0, 256), packed=(0, 512), ys=(0, 512), ws=None) == qlin.ERR_INVALID_ARG
 

@@ -172,3 +172,25 @@ def test_layer_graph_with_multi_matches_eager():
     assert qlin.read_device_status(ws) == qlin.OK
     ref = oracle_forward(qkv[1])
     assert_y_close(outs[1].cpu().numpy(), ref["y64"], "k in the graph")
+
+
+@pytest.mark.parametrize("fmt,kind,M,Ns,K,G", [("w4a8", "rmsnorm", 4, (272, 48), 384, 128),
+                                               ("w6a8", "none", 8, (144, 400), 160, 32),
+                                               ("w4a8", "swiglu", 1, (1040,), 1056, 16)])
+def test_multi_bias_matches_oracle(fmt, kind, M, Ns, K, G):
+    """A float bias per weight (some weights without one) against the oracle."""
+    base, cs = _multi_cases(fmt, kind, M, Ns, K, G, seed=3 * sum(Ns) + K)
+    db = device_case(base)
+    w = [device_case(c)["w"] for c in cs]
+    gen = torch.Generator().manual_seed(K)
+    biases = [torch.randn(N, generator=gen) * 4 if l % 2 == 0 else None for l, N in enumerate(Ns)]
+    ys = qlin.forward_multi(fmt, kind, w, list(Ns), K, G, flags=qlin.FLAG_PDL,
+                            bias=[None if b is None else b.to(DEV) for b in biases], **_acts(base, db))
+    for l, (c, y, b) in enumerate(zip(cs, ys, biases)):
+        ref = O.forward(c.fmt, c.kind, c.N, c.K, c.G, c.wbuf.numpy(), eps=c.eps,
+                        bias=None if b is None else b.numpy(),
+                        **{k: (inputs.bf16_bits(getattr(c, k)) if getattr(c, k) is not None else None)
+                           for k in ("x", "gate", "up")},
+                        gamma=None if c.gamma is None else c.gamma.numpy())
+        assert_y_close(y.cpu().numpy(), ref["y64"], f"weight {l} bias={b is not None}")
+

@@ -44,7 +44,8 @@ def test_hand_example_exact(fmt):
 # ---------------------------------------------------------------- repack
 @pytest.mark.parametrize("fmt,N,K,G", [
     ("w4a8", 144, 160, 32), ("w6a8", 144, 160, 32), ("w4a8", 256, 512, 128), ("w6a8", 16, 512, 256),
-    ("w4a8", 32, 256, 64), ("w6a8", 400, 384, 64), ("w4a8", 16, 32, 32),
+    ("w4a8", 32, 256, 64), ("w6a8", 400, 384, 64), ("w4a8", 16, 32, 32), ("w4a8", 144, 160, 16),
+    ("w6a8", 48, 96, 16),
 ])
 @pytest.mark.parametrize("small_ws", [False, True])
 def test_repack_roundtrip_bytes(fmt, N, K, G, small_ws):
@@ -132,7 +133,8 @@ def test_no_prologue_codes_exact_near_ties():
 # ---------------------------------------------------------------- exact group sums
 @pytest.mark.parametrize("fmt", ["w4a8", "w6a8"])
 @pytest.mark.parametrize("kind", ["none", "rmsnorm", "swiglu"])
-@pytest.mark.parametrize("M,N,K,G", [(1, 144, 160, 32), (8, 272, 384, 128), (3, 128, 512, 256), (6, 48, 1024, 64)])
+@pytest.mark.parametrize("M,N,K,G", [(1, 144, 160, 32), (8, 272, 384, 128), (3, 128, 512, 256), (6, 48, 1024, 64),
+                                     (5, 144, 160, 16), (8, 32, 256, 16)])
 def test_group_sums_exact(fmt, kind, M, N, K, G):
     c = inputs.make_case(fmt, kind, M, N, K, G, seed=M + N + K)
     d = device_case(c)
@@ -158,7 +160,8 @@ def test_group_sums_exact(fmt, kind, M, N, K, G):
 
 # ---------------------------------------------------------------- outputs, shapes and edges
 SHAPES = [(1, 16, 32, 32), (8, 16, 32, 32), (3, 144, 160, 32), (8, 272, 384, 128), (2, 128, 4096, 128),
-          (5, 400, 384, 64), (7, 128, 512, 256), (4, 1040, 1056, 32)]
+          (5, 400, 384, 64), (7, 128, 512, 256), (4, 1040, 1056, 32), (1, 16, 32, 16), (6, 400, 352, 16),
+          (8, 1040, 2048, 16)]
 
 
 @pytest.mark.parametrize("fmt", ["w4a8", "w6a8"])

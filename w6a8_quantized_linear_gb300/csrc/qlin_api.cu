@@ -51,10 +51,11 @@ const void* fwd_fn_g(int gi) {
     case 0: return fwd_fn<BITS, KIND, 32>();
     case 1: return fwd_fn<BITS, KIND, 64>();
     case 2: return fwd_fn<BITS, KIND, 128>();
-    default: return fwd_fn<BITS, KIND, 256>();
+    case 3: return fwd_fn<BITS, KIND, 256>();
+    default: return fwd_fn<BITS, KIND, 16>();
   }
 }
-int g_index(int64_t G) { return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : 3; }
+int g_index(int64_t G) { return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : G == 256 ? 3 : 4; }
 const void* forward_fn(int bits, int kind, int64_t G) {
   const int gi = g_index(G);
   if (bits == 6) return kind == 0 ? fwd_fn_g<6, 0>(gi) : kind == 1 ? fwd_fn_g<6, 1>(gi) : fwd_fn_g<6, 2>(gi);
@@ -74,7 +75,7 @@ qlin_status device_cache(DevCache** out) {
     if (e != cudaSuccess) return cuda_status(e);
     for (int bits : {4, 6})
       for (int kind = 0; kind < 3; kind++)
-        for (int64_t G : {32, 64, 128, 256}) {
+        for (int64_t G : {16, 32, 64, 128, 256}) {
           const void* fn = forward_fn(bits, kind, G);
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
           if (e != cudaSuccess) return cuda_status(e);
@@ -204,8 +205,8 @@ qlin_status check_shape_impl(int fmt, int64_t N, int64_t K, int64_t G) {
   } else {
     if (K % 32 != 0 || G % 16 != 0 || K % G != 0) return QLIN_ERR_INVALID_ARG;
   }
-  if (!(G == 32 || G == 64 || G == 128 || G == 256)) return QLIN_ERR_UNSUPPORTED;
-  if (N % 16 != 0 || K > MAX_K) return QLIN_ERR_UNSUPPORTED;
+  if (!(G == 16 || G == 32 || G == 64 || G == 128 || G == 256)) return QLIN_ERR_UNSUPPORTED;
+  if (N % 16 != 0 || K % 32 != 0 || K > MAX_K) return QLIN_ERR_UNSUPPORTED;
   return QLIN_OK;
 }
 
@@ -239,8 +240,9 @@ struct Outputs {  // test exports of a single-weight call
 // input: argument checks, the plan, the parameter block, the launch.
 qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int64_t K, int64_t G,
                          const void* const* packed, const void* x, const void* gate, const void* up,
-                         const float* gamma, float eps, float* const* ys, const Outputs& out, void* ws,
-                         size_t ws_bytes, unsigned flags, void* stream, bool debug, int64_t fault_unit = -1) {
+                         const float* gamma, float eps, float* const* ys, const float* const* biases,
+                         const Outputs& out, void* ws, size_t ws_bytes, unsigned flags, void* stream, bool debug,
+                         int64_t fault_unit = -1) {
   if (n < 1 || n > MAX_LIN || !Ns || !packed || !ys) return QLIN_ERR_INVALID_ARG;
   qlin_status st = QLIN_OK;
   int64_t NB = 0;
@@ -258,6 +260,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
     if (!packed[l] || !aligned(packed[l], 16)) return QLIN_ERR_INVALID_ARG;
     if (!debug && !ys[l]) return QLIN_ERR_INVALID_ARG;
     if (ys[l] && !aligned(ys[l], 4)) return QLIN_ERR_INVALID_ARG;
+    if (biases && biases[l] && !aligned(biases[l], 4)) return QLIN_ERR_INVALID_ARG;
   }
   if ((out.acc && !aligned(out.acc, 4)) || (out.s && !aligned(out.s, 4))) return QLIN_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return QLIN_ERR_INVALID_ARG;
@@ -279,6 +282,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
     if (Ns[l] == 0) continue;
     p.packed[nl] = static_cast<const uint8_t*>(packed[l]);
     p.y[nl] = ys[l];
+    p.bias[nl] = biases ? biases[l] : nullptr;
     p.N[nl] = Ns[l];
     p.T[nl] = (Ns[l] + TILE_N - 1) / TILE_N;
     p.blk0[nl + 1] = p.blk0[nl] + row_blocks(Ns[l]);
@@ -457,16 +461,16 @@ qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G, const void* packed,
                          const void* x, const void* gate, const void* up, const float* gamma, float eps, float* y,
                          void* ws, size_t ws_bytes, unsigned flags, void* stream) {
-  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, Outputs(), ws, ws_bytes,
-                      flags, stream, false);
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, nullptr, Outputs(), ws,
+                      ws_bytes, flags, stream, false);
 }
 
 qlin_status qlin_forward_multi(int fmt, int prologue, int M, int n, const int64_t* N, int64_t K, int64_t G,
                                const void* const* packed, const void* x, const void* gate, const void* up,
-                               const float* gamma, float eps, float* const* y, void* ws, size_t ws_bytes,
-                               unsigned flags, void* stream) {
-  return forward_impl(fmt, prologue, M, n, N, K, G, packed, x, gate, up, gamma, eps, y, Outputs(), ws, ws_bytes,
-                      flags, stream, false);
+                               const float* gamma, float eps, float* const* y, const float* const* bias, void* ws,
+                               size_t ws_bytes, unsigned flags, void* stream) {
+  return forward_impl(fmt, prologue, M, n, N, K, G, packed, x, gate, up, gamma, eps, y, bias, Outputs(), ws,
+                      ws_bytes, flags, stream, false);
 }
 
 qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, int64_t* ctas, int64_t* units,
@@ -507,8 +511,8 @@ qlin_status qlin_debug_forward(int fmt, int prologue, int M, int64_t N, int64_t 
   o.acc = acc;
   o.q = q;
   o.s = s;
-  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, o, ws, ws_bytes, 0, stream,
-                      true);
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, nullptr, o, ws, ws_bytes, 0,
+                      stream, true);
 }
 
 qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
@@ -516,8 +520,8 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
                                      const float* gamma, float eps, float* y, void* ws, size_t ws_bytes,
                                      int64_t unit, void* stream) {
   if (unit < 0) return QLIN_ERR_INVALID_ARG;
-  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, Outputs(), ws, ws_bytes, 0,
-                      stream, false, unit);
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, nullptr, Outputs(), ws,
+                      ws_bytes, 0, stream, false, unit);
 }
 
 qlin_status qlin_forward_noalloc(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
@@ -532,7 +536,7 @@ qlin_status qlin_forward_noalloc(int fmt, int prologue, int M, int64_t N, int64_
   void* ws = nullptr;
   st = noalloc_scratch(&ws);
   if (st != QLIN_OK) return st;
-  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, Outputs(), ws,
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, nullptr, Outputs(), ws,
                       NOALLOC_SCRATCH_BYTES, flags, stream, false);
 }
 

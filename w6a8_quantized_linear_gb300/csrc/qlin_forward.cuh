@@ -55,6 +55,7 @@ struct FwdParams {
   int n_lin;
   const uint8_t* packed[MAX_LIN];
   float* y[MAX_LIN];          // [M, N[l]]
+  const float* bias[MAX_LIN]; // fp32 [N[l]] or null
   int64_t N[MAX_LIN], T[MAX_LIN];
   int64_t blk0[MAX_LIN + 1];
   const __nv_bfloat16* x;     // NONE, RMSNORM: [M, K]
@@ -219,12 +220,16 @@ __device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uin
 
 template <int BITS, int KIND, int G>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
-  constexpr int KB = G > 128 ? G : 128;  // k per stream unit
-  constexpr int SG = G < 128 ? G : 128;  // k per MMA sub-group (exact chains)
-  constexpr int SPG = G / SG;            // sub-groups per group
-  constexpr int GPU = KB / G;            // groups per full unit
-  constexpr int PPS = SG / PAIR_K;       // 32-wide pairs per sub-group
-  constexpr int SEG = SG / 8;            // lanes whose 8 k make one sub-group (quantisation pass)
+  // G = 16: each 16-wide k-step is a group, so the two chains of a 32-wide
+  // pair are two groups and a sub-group (the unit of chain start values) is
+  // one pair.
+  constexpr bool PER_STEP = G < PAIR_K;
+  constexpr int KB = G > 128 ? G : 128;                          // k per stream unit
+  constexpr int SG = PER_STEP ? PAIR_K : (G < 128 ? G : 128);    // k per MMA sub-group (exact chains)
+  constexpr int SPG = PER_STEP ? 1 : G / SG;                     // sub-groups per group
+  constexpr int GPU = KB / G;                                    // groups per full unit
+  constexpr int PPS = SG / PAIR_K;                               // 32-wide pairs per sub-group
+  constexpr int SEG = SG / 8;                                    // lanes whose 8 k make one sub-group
   constexpr int PB = BITS == 6 ? 384 : 256;
 
   extern __shared__ __align__(128) uint8_t smem[];
@@ -250,12 +255,14 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   // indexed at run time)
   const uint8_t* packed = p.packed[0];
   float* y = p.y[0];
+  const float* bias = p.bias[0];
   int64_t N = p.N[0], T = p.T[0], blk_first = 0;
 #pragma unroll
   for (int l = 1; l < MAX_LIN; l++) {
     if (l < p.n_lin && (int64_t)blockIdx.y >= p.blk0[l]) {
       packed = p.packed[l];
       y = p.y[l];
+      bias = p.bias[l];
       N = p.N[l];
       T = p.T[l];
       blk_first = p.blk0[l];
@@ -534,6 +541,51 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     const int slab_bytes = last ? slast : sfull;
     const uint8_t* c0p = unit + (last ? clast : cfull);
     const uint8_t* c1p = c0p + slab_bytes;
+    if constexpr (PER_STEP) {
+      // chain A of pair pr is group 2 pr, chain B group 2 pr + 1: each chain is
+      // one MMA that starts at its group's start value
+#pragma unroll
+      for (int pr = 0; pr < KB / PAIR_K; pr++) {
+        const float4 sA = *reinterpret_cast<const float4*>(bblk + CIN + pr * 128 + tq * 16);
+        const float4 sB = *reinterpret_cast<const float4*>(bblk + CIN + pr * 128 + 64 + tq * 16);
+        const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * BPM + blane);
+        float a0[4], b0[4], a1[4], b1[4];
+        slab_pair<BITS>(c0p + pr * PB, lane, bq, true, sA, sB, base, a0, b0);
+        slab_pair<BITS>(c1p + pr * PB, lane, bq, true, sA, sB, base, a1, b1);
+#pragma unroll
+        for (int st = 0; st < 2; st++) {
+          const int gi = 2 * pr + st;
+          const float* d0 = st == 0 ? a0 : b0;
+          const float* d1 = st == 0 ? a1 : b1;
+          float2 sw0 = *reinterpret_cast<const float2*>(unit + soff0 + gi * sgrp);
+          float2 sw1 = *reinterpret_cast<const float2*>(unit + soff0 + gi * sgrp + 64);
+          if (gi >= ng) sw0 = sw1 = make_float2(0.f, 0.f);  // group past a narrower unit
+          yacc[0][0] = __fmaf_rn(sw0.x, d0[0], yacc[0][0]);
+          yacc[0][1] = __fmaf_rn(sw0.x, d0[1], yacc[0][1]);
+          yacc[0][2] = __fmaf_rn(sw0.y, d0[2], yacc[0][2]);
+          yacc[0][3] = __fmaf_rn(sw0.y, d0[3], yacc[0][3]);
+          yacc[1][0] = __fmaf_rn(sw1.x, d1[0], yacc[1][0]);
+          yacc[1][1] = __fmaf_rn(sw1.x, d1[1], yacc[1][1]);
+          yacc[1][2] = __fmaf_rn(sw1.y, d1[2], yacc[1][2]);
+          yacc[1][3] = __fmaf_rn(sw1.y, d1[3], yacc[1][3]);
+          if (p.acc_out && gi < ng) {  // test export: exact group sums
+            const int64_t NG = p.K / G, gg = ((j0 + i) * KB) / G + gi;
+#pragma unroll
+            for (int a = 0; a < 2; a++) {
+              if (sl0 + a >= nslab) continue;
+              const float* d = a == 0 ? d0 : d1;
+              const int64_t n0 = t * TILE_N + (sl0 + a) * SLAB + g;
+#pragma unroll
+              for (int e = 0; e < 4; e++) {
+                const int mm = 2 * tq + (e & 1);
+                const float v = e < 2 ? d[e] : d[e] * 0.0625f;
+                if (mm < M) p.acc_out[((int64_t)mm * N + n0 + (e >> 1) * 8) * NG + gg] = __float2int_rn(v);
+              }
+            }
+          }
+        }
+      }
+    } else {
 #pragma unroll
     for (int gi = 0; gi < GPU; gi++) {
       float d0[4], d1[4];
@@ -583,6 +635,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         }
       }
     }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[s]);
     bblk += p.bbf;
@@ -630,13 +683,14 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         const int slab = 2 * (w_src & 3) + a;
         if (slab * SLAB >= Rt) continue;
         const int64_t n = tt * TILE_N + slab * SLAB + gs;
+        const float b0 = bias ? bias[n] : 0.f, b8 = bias ? bias[n + 8] : 0.f;
         if (2 * ts < M) {
-          y[(int64_t)(2 * ts) * N + n] = sm0 * v[4 * a + 0];
-          y[(int64_t)(2 * ts) * N + n + 8] = sm0 * v[4 * a + 2];
+          y[(int64_t)(2 * ts) * N + n] = __fmaf_rn(sm0, v[4 * a + 0], b0);
+          y[(int64_t)(2 * ts) * N + n + 8] = __fmaf_rn(sm0, v[4 * a + 2], b8);
         }
         if (2 * ts + 1 < M) {
-          y[(int64_t)(2 * ts + 1) * N + n] = sm1 * v[4 * a + 1];
-          y[(int64_t)(2 * ts + 1) * N + n + 8] = sm1 * v[4 * a + 3];
+          y[(int64_t)(2 * ts + 1) * N + n] = __fmaf_rn(sm1, v[4 * a + 1], b0);
+          y[(int64_t)(2 * ts + 1) * N + n + 8] = __fmaf_rn(sm1, v[4 * a + 3], b8);
         }
       }
     }

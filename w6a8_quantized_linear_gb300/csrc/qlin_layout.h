@@ -57,7 +57,7 @@ QL_HD int64_t unit_bytes(int bits, int64_t R, int64_t W, int64_t G) {
 // an MMA column depends on its own B column only, and those columns are never
 // written out.
 QL_HD int64_t bpair_bytes(int64_t M) { return 64 * M + 16; }
-QL_HD int64_t sub_group(int64_t G) { return G < 128 ? G : 128; }
+QL_HD int64_t sub_group(int64_t G) { return G < 32 ? 32 : (G < 128 ? G : 128); }
 QL_HD int64_t bblock_bytes(int64_t W, int64_t G, int64_t M) {
   return (W / 32) * bpair_bytes(M) + (W / sub_group(G)) * 128;
 }

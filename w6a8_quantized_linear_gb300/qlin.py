@@ -56,7 +56,7 @@ def lib() -> ctypes.CDLL:
                 "qlin_forward": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz,
                                       ctypes.c_uint, vp]),
                 "qlin_forward_multi": (st, [i32, i32, i32, i32, vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float,
-                                            vp, vp, sz, ctypes.c_uint, vp]),
+                                            vp, vp, vp, sz, ctypes.c_uint, vp]),
                 "qlin_forward_launch_info": (st, [i32, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                                   ctypes.POINTER(i64)]),
                 "qlin_read_device_status": (st, [vp, vp]),
@@ -173,10 +173,11 @@ MAX_MULTI = 8
 
 
 def forward_multi(fmt, prologue, packed: list, N: list, K: int, G: int, x=None, gate=None, up=None, gamma=None,
-                  eps: float = 1e-6, y: list | None = None, ws: torch.Tensor | None = None, flags: int = 0,
-                  stream=None) -> list:
+                  eps: float = 1e-6, y: list | None = None, bias: list | None = None,
+                  ws: torch.Tensor | None = None, flags: int = 0, stream=None) -> list:
     """Several weights on one shared activation in one launch: y[l] = packed[l] x
-    quantised prologue(activation).  Returns the list of fp32 [M, N[l]] outputs."""
+    quantised prologue(activation) (+ bias[l], fp32 [N[l]], where given).
+    Returns the list of fp32 [M, N[l]] outputs."""
     act = gate if _pro(prologue) == 2 else x
     M = act.shape[0]
     n = len(packed)
@@ -190,9 +191,11 @@ def forward_multi(fmt, prologue, packed: list, N: list, K: int, G: int, x=None, 
     n_arr = (ctypes.c_int64 * n)(*N)
     p_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in packed])
     y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in y])
+    b_arr = None if bias is None else (ctypes.c_void_p * n)(*[_ptr(t) for t in bias])
     _check(lib().qlin_forward_multi(_fmt(fmt), _pro(prologue), M, n, ctypes.cast(n_arr, ctypes.c_void_p), K, G,
                                     ctypes.cast(p_arr, ctypes.c_void_p), _ptr(x), _ptr(gate), _ptr(up), _ptr(gamma),
-                                    float(eps), ctypes.cast(y_arr, ctypes.c_void_p), _ptr(ws), ws.numel(), flags,
+                                    float(eps), ctypes.cast(y_arr, ctypes.c_void_p),
+                                    None if b_arr is None else ctypes.cast(b_arr, ctypes.c_void_p), _ptr(ws), ws.numel(), flags,
                                     _stream(stream)), "forward_multi")
     return y
 
