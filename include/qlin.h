@@ -42,8 +42,9 @@
  *    read back by qlin_read_device_status; the kernel returns instead of
  *    hanging.
  *  - fmt is QLIN_W4A8 or QLIN_W6A8; b = 4 or 6 bits per code.
- *  - Backend limits beyond [OPT] (QLIN_ERR_UNSUPPORTED): G in {16, 32, 64,
- *    128, 256}, K % 32 == 0, N % 16 == 0, K <= 65536, M <= 8.
+ *  - Backend limits beyond [OPT] (QLIN_ERR_UNSUPPORTED): G in {4, 8, 16, 32,
+ *    64, 128, 256} (4 and 8 for 4-bit codes, as the format allows),
+ *    K % 32 == 0, N % 16 == 0, K <= 65536, M <= 8.
  */
 #ifndef QLIN_H_
 #define QLIN_H_

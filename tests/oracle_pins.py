@@ -131,6 +131,15 @@ def check_forward_bruteforce(O, seed=2):
             if bias is not None:
                 yb = yb + bias.astype(np.float64)[None, :]
             assert np.allclose(r["y64"], yb, rtol=1e-12, atol=1e-12 * np.abs(yb).max()), (fmt, N, K, G)
+    for (N, K, G) in ((16, 32, 8), (16, 64, 4), (32, 96, 8)):  # groups below 16: 4-bit codes only
+        gen = torch.Generator().manual_seed(rng.randint(0, 10**6))
+        x = torch.randn(3, K, generator=gen).to(torch.bfloat16)
+        codes = torch.randint(0, 256, (N * K // 2,), generator=gen, dtype=torch.uint8).numpy()
+        sw = torch.empty(N * (K // G)).uniform_(0.01, 0.02, generator=gen).numpy().astype("<f4")
+        wbuf = np.concatenate([codes, sw.view(np.uint8)])
+        r = O.forward("w4a8", "none", N, K, G, wbuf, x=bits_of(x))
+        yb = _bruteforce_y("w4a8", N, K, G, wbuf, r["q"], r["s"])
+        assert np.allclose(r["y64"], yb, rtol=1e-12, atol=1e-12 * np.abs(yb).max()), (N, K, G)
 
 
 def check_quantize(O, seed=3):

@@ -54,8 +54,9 @@ def test_version_and_status_strings(L):
     ("w4a8", 16, 64, 16, qlin.OK),                 # one group per 16-wide k-step
     ("w6a8", 32, 96, 16, qlin.OK),
     ("w4a8", 16, 48, 16, qlin.ERR_UNSUPPORTED),    # legal, K % 32 != 0 (this backend works in 32-wide pairs)
-    ("w4a8", 16, 64, 8, qlin.ERR_UNSUPPORTED),     # legal, below this backend's G range
-    ("w4a8", 16, 64, 4, qlin.ERR_UNSUPPORTED),
+    ("w4a8", 16, 64, 8, qlin.OK),                  # groups of 8: m16n8k8 halves
+    ("w4a8", 16, 64, 4, qlin.OK),                  # groups of 4: masked halves
+    ("w4a8", 16, 48, 4, qlin.ERR_UNSUPPORTED),     # legal, K % 32 != 0
     ("w4a8", 16, 1024, 512, qlin.ERR_UNSUPPORTED),
     ("w4a8", 24, 256, 32, qlin.ERR_UNSUPPORTED),   # N % 16
     ("w4a8", 16, 131072, 128, qlin.ERR_UNSUPPORTED),

@@ -45,7 +45,7 @@ def test_hand_example_exact(fmt):
 @pytest.mark.parametrize("fmt,N,K,G", [
     ("w4a8", 144, 160, 32), ("w6a8", 144, 160, 32), ("w4a8", 256, 512, 128), ("w6a8", 16, 512, 256),
     ("w4a8", 32, 256, 64), ("w6a8", 400, 384, 64), ("w4a8", 16, 32, 32), ("w4a8", 144, 160, 16),
-    ("w6a8", 48, 96, 16),
+    ("w6a8", 48, 96, 16), ("w4a8", 144, 160, 8), ("w4a8", 48, 96, 4),
 ])
 @pytest.mark.parametrize("small_ws", [False, True])
 def test_repack_roundtrip_bytes(fmt, N, K, G, small_ws):
@@ -156,6 +156,32 @@ def test_group_sums_exact(fmt, kind, M, N, K, G):
         corr = np.einsum("mgk,ngk->mng", dq, L)
         assert np.array_equal(acc_h, ref["acc"] + corr)
     assert_y_close(y.cpu().numpy(), ref["y64"], f"{fmt} {kind}")
+
+
+@pytest.mark.parametrize("kind", ["none", "rmsnorm", "swiglu"])
+@pytest.mark.parametrize("M,N,K,G", [(1, 144, 160, 8), (8, 272, 384, 8), (3, 144, 160, 4), (8, 48, 512, 4),
+                                     (5, 1040, 1056, 8)])
+def test_small_groups_exact_sums_and_outputs(kind, M, N, K, G):
+    """Groups of 8 and 4 (4-bit codes): exact group sums and outputs."""
+    c = inputs.make_case("w4a8", kind, M, N, K, G, seed=11 * M + N + K + G)
+    d = device_case(c)
+    r = qlin.debug_forward("w4a8", kind, d["w"], N, K, G, x=d["x"], gate=d["gate"], up=d["up"], gamma=d["gamma"],
+                           eps=c.eps)
+    ref = oracle_forward(c)
+    acc_h = r["acc"].cpu().numpy().astype(np.int64)
+    qg = r["q"].cpu().numpy().astype(np.int64)
+    if kind == "none":
+        assert np.array_equal(qg, ref["q"])
+        assert np.array_equal(acc_h, ref["acc"])
+    else:
+        boundary_ok(qg, ref)
+        dq = (qg - ref["q"]).reshape(M, K // G, G)
+        codes, _ = O.unpack_file("w4a8", N, K, G, c.wbuf.numpy())
+        L = (codes - 8).reshape(N, K // G, G)
+        assert np.array_equal(acc_h, ref["acc"] + np.einsum("mgk,ngk->mng", dq, L))
+    assert_y_close(r["y"].cpu().numpy(), ref["y64"], f"G={G} {kind}")
+    y = gpu_forward(c, d, flags=qlin.FLAG_PDL)
+    assert torch.equal(y, r["y"])
 
 
 # ---------------------------------------------------------------- outputs, shapes and edges

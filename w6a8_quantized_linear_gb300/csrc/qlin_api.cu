@@ -52,10 +52,18 @@ const void* fwd_fn_g(int gi) {
     case 1: return fwd_fn<BITS, KIND, 64>();
     case 2: return fwd_fn<BITS, KIND, 128>();
     case 3: return fwd_fn<BITS, KIND, 256>();
-    default: return fwd_fn<BITS, KIND, 16>();
+    case 4: return fwd_fn<BITS, KIND, 16>();
+    default: break;
   }
+  if constexpr (BITS == 4) {  // groups of 8 and 4 exist for 4-bit codes only
+    if (gi == 5) return fwd_fn<BITS, KIND, 8>();
+    return fwd_fn<BITS, KIND, 4>();
+  }
+  return nullptr;
 }
-int g_index(int64_t G) { return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : G == 256 ? 3 : 4; }
+int g_index(int64_t G) {
+  return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : G == 256 ? 3 : G == 16 ? 4 : G == 8 ? 5 : 6;
+}
 const void* forward_fn(int bits, int kind, int64_t G) {
   const int gi = g_index(G);
   if (bits == 6) return kind == 0 ? fwd_fn_g<6, 0>(gi) : kind == 1 ? fwd_fn_g<6, 1>(gi) : fwd_fn_g<6, 2>(gi);
@@ -75,8 +83,9 @@ qlin_status device_cache(DevCache** out) {
     if (e != cudaSuccess) return cuda_status(e);
     for (int bits : {4, 6})
       for (int kind = 0; kind < 3; kind++)
-        for (int64_t G : {16, 32, 64, 128, 256}) {
+        for (int64_t G : {4, 8, 16, 32, 64, 128, 256}) {
           const void* fn = forward_fn(bits, kind, G);
+          if (!fn) continue;
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
           if (e != cudaSuccess) return cuda_status(e);
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -205,7 +214,7 @@ qlin_status check_shape_impl(int fmt, int64_t N, int64_t K, int64_t G) {
   } else {
     if (K % 32 != 0 || G % 16 != 0 || K % G != 0) return QLIN_ERR_INVALID_ARG;
   }
-  if (!(G == 16 || G == 32 || G == 64 || G == 128 || G == 256)) return QLIN_ERR_UNSUPPORTED;
+  if (!(G == 4 || G == 8 || G == 16 || G == 32 || G == 64 || G == 128 || G == 256)) return QLIN_ERR_UNSUPPORTED;
   if (N % 16 != 0 || K % 32 != 0 || K > MAX_K) return QLIN_ERR_UNSUPPORTED;
   return QLIN_OK;
 }

@@ -218,12 +218,52 @@ __device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uin
   }
 }
 
+// The A registers of one 32-wide k pair of one slab: a = k-step A, b = k-step B.
+template <int BITS>
+__device__ __forceinline__ void unpack_pair(const uint8_t* cp, int lane, uint32_t base, uint32_t (&a)[4],
+                                            uint32_t (&b)[4]) {
+  const uint2 w = *reinterpret_cast<const uint2*>(cp + lane * 8);
+  uint32_t hA01 = 0, hA23 = 0, hB01 = 0, hB23 = 0;
+  if (BITS == 6) {
+    const uint32_t h = *reinterpret_cast<const uint32_t*>(cp + 256 + lane * 4);
+    hA01 = h << 4;
+    hA23 = h << 2;
+    hB01 = h >> 4;
+    hB23 = h >> 6;
+  }
+  unpack_step<BITS>(w.x, hA01, hA23, base, a);
+  unpack_step<BITS>(w.y, hB01, hB23, base, b);
+}
+
+// Group gp of a pair whose groups are narrower than the pair (GPP = 32 / G
+// groups): one MMA from the group's start value ci.
+//   G = 16: the two 16-wide k-steps (m16n8k16);
+//   G = 8: the four 8-wide halves (m16n8k8: registers 0/1 hold k 0..7 of a
+//          step, registers 2/3 k 8..15);
+//   G = 4: each 8-wide half twice, with the B fragment kept only in the
+//          lanes that hold k 0..3 (t < 2) or k 4..7 (t >= 2).
+template <int GPP>
+__device__ __forceinline__ void group_mma(const uint32_t (&a)[4], const uint32_t (&b)[4], int gp, bool lo_lanes,
+                                          const uint4& bq, const float4& ci, float (&d)[4]) {
+  if constexpr (GPP == 2) {
+    if (gp == 0) mma_f16_16816_c(d, a[0], a[1], a[2], a[3], bq.x, bq.y, ci.x, ci.y, ci.z, ci.w);
+    else mma_f16_16816_c(d, b[0], b[1], b[2], b[3], bq.z, bq.w, ci.x, ci.y, ci.z, ci.w);
+  } else {
+    const int half = GPP == 4 ? gp : gp >> 1;  // which 8-wide half of the pair: A lo, A hi, B lo, B hi
+    const uint32_t r0 = half == 0 ? a[0] : half == 1 ? a[2] : half == 2 ? b[0] : b[2];
+    const uint32_t r1 = half == 0 ? a[1] : half == 1 ? a[3] : half == 2 ? b[1] : b[3];
+    uint32_t bf = half == 0 ? bq.x : half == 1 ? bq.y : half == 2 ? bq.z : bq.w;
+    if (GPP == 8) bf = ((gp & 1) == 0) == lo_lanes ? bf : 0u;
+    mma_f16_1688_c(d, r0, r1, bf, ci);
+  }
+}
+
 template <int BITS, int KIND, int G>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
-  // G = 16: each 16-wide k-step is a group, so the two chains of a 32-wide
-  // pair are two groups and a sub-group (the unit of chain start values) is
-  // one pair.
+  // G < 32: groups are narrower than a 32-wide pair; each group is its own
+  // chain (one MMA) with its own start value, GPP groups per pair.
   constexpr bool PER_STEP = G < PAIR_K;
+  constexpr int GPP = PER_STEP ? PAIR_K / G : 1;
   constexpr int KB = G > 128 ? G : 128;                          // k per stream unit
   constexpr int SG = PER_STEP ? PAIR_K : (G < 128 ? G : 128);    // k per MMA sub-group (exact chains)
   constexpr int SPG = PER_STEP ? 1 : G / SG;                     // sub-groups per group
@@ -438,10 +478,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       const int kin = (int)(kl - jl * KB);
       uint8_t* blk = bop + jl * p.bbf;
       const int pr = kin / PAIR_K, step = (kin / KSTEP) & 1, half = (kin % KSTEP) >= 8;
-      float rowsum[MAX_M];
+      float rowsum[MAX_M], rowlo[MAX_M];  // rowlo: k 0..3 of the 8 (groups of 4)
 #pragma unroll
       for (int m = 0; m < MAX_M; m++) {
         rowsum[m] = 0.f;
+        rowlo[m] = 0.f;
         if (inb && m < M) {
           float qf[8];
           if (valid) {
@@ -461,6 +502,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
               const float q = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);  // round half to even
               qf[e] = q;
               rowsum[m] += q;
+              if (G == 4 && e < 4) rowlo[m] += q;
             }
             if (p.q_out && blockIdx.y == 0) {
 #pragma unroll
@@ -477,6 +519,24 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
           }
         }
       }
+      if constexpr (G < 16) {
+        // a thread's 8 k hold one group (G = 8) or two (G = 4): no exchange
+        if (inb) {
+#pragma unroll
+          for (int hq = 0; hq < 8 / G; hq++) {
+            const int gp = (kin % PAIR_K) / G + hq;
+            float* cin = reinterpret_cast<float*>(blk + CIN + (pr * GPP + gp) * 64);
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+              float s0 = 0.f, s1 = 0.f;
+              if (2 * t < M) s0 = G == 4 ? (hq == 0 ? rowlo[2 * t] : rowsum[2 * t] - rowlo[2 * t]) : rowsum[2 * t];
+              if (2 * t + 1 < M)
+                s1 = G == 4 ? (hq == 0 ? rowlo[2 * t + 1] : rowsum[2 * t + 1] - rowlo[2 * t + 1]) : rowsum[2 * t + 1];
+              reinterpret_cast<float4*>(cin)[t] = make_float4(fg * s0, fg * s1, fg8 * s0, fg8 * s1);
+            }
+          }
+        }
+      } else {
       // lanes [SEG*i, SEG*(i+1)) hold one sub-group's 8-k slices; lane bit 1
       // is the k-step, so summing over the other bits gives each chain's sum
 #pragma unroll
@@ -496,6 +556,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
           const float s1 = 2 * t + 1 < M ? rowsum[2 * t + 1] : 0.f;
           reinterpret_cast<float4*>(cin)[t] = make_float4(fg * s0, fg * s1, fg8 * s0, fg8 * s1);
         }
+      }
       }
     }
   }
@@ -542,38 +603,29 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     const uint8_t* c0p = unit + (last ? clast : cfull);
     const uint8_t* c1p = c0p + slab_bytes;
     if constexpr (PER_STEP) {
-      // chain A of pair pr is group 2 pr, chain B group 2 pr + 1: each chain is
-      // one MMA that starts at its group's start value
+      // groups narrower than a pair: each group is one MMA from its own start
+      // value, scaled on its own
 #pragma unroll
       for (int pr = 0; pr < KB / PAIR_K; pr++) {
-        const float4 sA = *reinterpret_cast<const float4*>(bblk + CIN + pr * 128 + tq * 16);
-        const float4 sB = *reinterpret_cast<const float4*>(bblk + CIN + pr * 128 + 64 + tq * 16);
         const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * BPM + blane);
-        float a0[4], b0[4], a1[4], b1[4];
-        slab_pair<BITS>(c0p + pr * PB, lane, bq, true, sA, sB, base, a0, b0);
-        slab_pair<BITS>(c1p + pr * PB, lane, bq, true, sA, sB, base, a1, b1);
 #pragma unroll
-        for (int st = 0; st < 2; st++) {
-          const int gi = 2 * pr + st;
-          const float* d0 = st == 0 ? a0 : b0;
-          const float* d1 = st == 0 ? a1 : b1;
-          float2 sw0 = *reinterpret_cast<const float2*>(unit + soff0 + gi * sgrp);
-          float2 sw1 = *reinterpret_cast<const float2*>(unit + soff0 + gi * sgrp + 64);
-          if (gi >= ng) sw0 = sw1 = make_float2(0.f, 0.f);  // group past a narrower unit
-          yacc[0][0] = __fmaf_rn(sw0.x, d0[0], yacc[0][0]);
-          yacc[0][1] = __fmaf_rn(sw0.x, d0[1], yacc[0][1]);
-          yacc[0][2] = __fmaf_rn(sw0.y, d0[2], yacc[0][2]);
-          yacc[0][3] = __fmaf_rn(sw0.y, d0[3], yacc[0][3]);
-          yacc[1][0] = __fmaf_rn(sw1.x, d1[0], yacc[1][0]);
-          yacc[1][1] = __fmaf_rn(sw1.x, d1[1], yacc[1][1]);
-          yacc[1][2] = __fmaf_rn(sw1.y, d1[2], yacc[1][2]);
-          yacc[1][3] = __fmaf_rn(sw1.y, d1[3], yacc[1][3]);
-          if (p.acc_out && gi < ng) {  // test export: exact group sums
-            const int64_t NG = p.K / G, gg = ((j0 + i) * KB) / G + gi;
+        for (int a = 0; a < 2; a++) {
+          uint32_t ra[4], rb[4];
+          unpack_pair<BITS>((a == 0 ? c0p : c1p) + pr * PB, lane, base, ra, rb);
 #pragma unroll
-            for (int a = 0; a < 2; a++) {
-              if (sl0 + a >= nslab) continue;
-              const float* d = a == 0 ? d0 : d1;
+          for (int gp = 0; gp < GPP; gp++) {
+            const int gi = pr * GPP + gp;
+            const float4 ci = *reinterpret_cast<const float4*>(bblk + CIN + (pr * GPP + gp) * 64 + tq * 16);
+            float d[4];
+            group_mma<GPP>(ra, rb, gp, tq < 2, bq, ci, d);
+            float2 sw = *reinterpret_cast<const float2*>(unit + soff0 + gi * sgrp + a * 64);
+            if (gi >= ng) sw = make_float2(0.f, 0.f);  // group past a narrower unit
+            yacc[a][0] = __fmaf_rn(sw.x, d[0], yacc[a][0]);
+            yacc[a][1] = __fmaf_rn(sw.x, d[1], yacc[a][1]);
+            yacc[a][2] = __fmaf_rn(sw.y, d[2], yacc[a][2]);
+            yacc[a][3] = __fmaf_rn(sw.y, d[3], yacc[a][3]);
+            if (p.acc_out && gi < ng && sl0 + a < nslab) {  // test export: exact group sums
+              const int64_t NG = p.K / G, gg = ((j0 + i) * KB) / G + gi;
               const int64_t n0 = t * TILE_N + (sl0 + a) * SLAB + g;
 #pragma unroll
               for (int e = 0; e < 4; e++) {

@@ -58,9 +58,10 @@ QL_HD int64_t unit_bytes(int bits, int64_t R, int64_t W, int64_t G) {
 // written out.
 QL_HD int64_t bpair_bytes(int64_t M) { return 64 * M + 16; }
 QL_HD int64_t sub_group(int64_t G) { return G < 32 ? 32 : (G < 128 ? G : 128); }
-QL_HD int64_t bblock_bytes(int64_t W, int64_t G, int64_t M) {
-  return (W / 32) * bpair_bytes(M) + (W / sub_group(G)) * 128;
-}
+// start values: 128 bytes per sub-group, or 64 bytes per group when groups
+// are narrower than a 32-wide pair
+QL_HD int64_t cin_bytes(int64_t W, int64_t G) { return G < 32 ? (W / G) * 64 : (W / sub_group(G)) * 128; }
+QL_HD int64_t bblock_bytes(int64_t W, int64_t G, int64_t M) { return (W / 32) * bpair_bytes(M) + cin_bytes(W, G); }
 
 struct Geo {
   int bits;
