@@ -66,7 +66,7 @@ import numpy as np
 __all__ = [
     "BITS", "code_offset", "file_code_bytes", "file_scale_bytes", "file_bytes",
     "unpack_file", "pack_file", "bf16_bits_to_f64", "prologue", "quantize_rows",
-    "group_acc", "forward", "STREAM_TN", "stream_kb", "unpack_stream",
+    "group_acc", "forward", "forward_moe", "STREAM_TN", "stream_kb", "unpack_stream",
 ]
 
 BITS = {"w4a8": 4, "w6a8": 6}
@@ -268,6 +268,38 @@ def forward(fmt: str, kind: str, N: int, K: int, G: int, buf, x=None, gate=None,
         b = np.asarray(bias, dtype=np.float32).astype(np.float64)
         y64 = y64 + (b if cols is None else b[np.asarray(cols)])[None, :]
     return {"y": y64.astype(np.float32), "y64": y64, "q": q, "s": s, "v": v, "acc": acc, "a": a}
+
+
+def forward_moe(fmt: str, kind: str, E: int, N: int, K: int, G: int, bank, ids, x=None, gate=None, up=None,
+                gamma=None, eps: float = 1e-6, bias=None, rows=None) -> dict:
+    """Expert bank: y[m, j, :] = expert ids[m, j] applied to token m.
+
+    "Comfy Quantization Formats", section "Embeddings and MoE": an expert
+    bank's weights and per-expert scales carry a leading expert dimension E;
+    a grouped W4A8 / W6A8 bank may be stored with expert and output rows
+    flattened to E * N (so ``bank`` is the checkpoint layout of an [E * N, K]
+    weight); the optional bias is [E, N].  Readings: every token is
+    quantised once, as for a plain linear; ids [M, topk] selects, for each
+    token, the experts whose outputs are returned (no routing weights are
+    applied).  ``rows`` limits the check to listed output rows n < N.
+    Returns y [M, topk, N'] (float64 and fp32) and the token codes.
+    """
+    ids = np.asarray(ids, dtype=np.int64)
+    M, topk = ids.shape
+    sel = np.arange(N) if rows is None else np.asarray(rows)
+    used = sorted(set(int(e) for e in ids.ravel()))
+    y64 = np.zeros((M, topk, sel.size))
+    q = s = None
+    for e in used:
+        cols = e * N + sel
+        r = forward(fmt, kind, E * N, K, G, bank, x=x, gate=gate, up=up, gamma=gamma, eps=eps, cols=cols,
+                    bias=None if bias is None else np.asarray(bias, np.float32).reshape(E * N))
+        q, s = r["q"], r["s"]
+        for m in range(M):
+            for j in range(topk):
+                if ids[m, j] == e:
+                    y64[m, j] = r["y64"][m]
+    return {"y": y64.astype(np.float32), "y64": y64, "q": q, "s": s}
 
 
 # ----------------------------------------------------------------------------

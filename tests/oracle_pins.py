@@ -320,3 +320,29 @@ def check_bias(O, seed=9):
                          cols=cols)
         assert np.array_equal(part["y64"], full["y64"][:, cols]), fmt
 
+
+def check_moe(O, seed=10):
+    """An expert bank is E separate weights stacked along the output rows:
+    each routed (token, slot) equals a plain forward of that expert's own
+    weight (packed on its own) for that token alone, bias included; a token
+    routed to one expert twice gets the same rows in both slots."""
+    rng = np.random.default_rng(seed)
+    for fmt in ("w4a8", "w6a8"):
+        b = {"w4a8": 4, "w6a8": 6}[fmt]
+        E, N, K, G = 5, 32, 64, 32
+        codes = rng.integers(0, 1 << b, (E * N, K))
+        sw = rng.uniform(0.01, 0.02, (E * N, K // G)).astype(np.float32)
+        bias = rng.normal(size=(E, N)).astype(np.float32)
+        bank = O.pack_file(fmt, codes, sw)
+        x = torch.randn(3, K, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+        gamma = rng.uniform(0.5, 1.5, K).astype(np.float32)
+        ids = np.array([[4, 1], [0, 0], [2, 4]])
+        r = O.forward_moe(fmt, "rmsnorm", E, N, K, G, bank, ids, x=bits_of(x), gamma=gamma, bias=bias)
+        for m in range(3):
+            for j in range(2):
+                e = ids[m, j]
+                own = O.pack_file(fmt, codes[e * N:(e + 1) * N], sw[e * N:(e + 1) * N])
+                one = O.forward(fmt, "rmsnorm", N, K, G, own, x=bits_of(x[m:m + 1]), gamma=gamma, bias=bias[e])
+                assert np.array_equal(r["y64"][m, j], one["y64"][0]), (fmt, m, j)
+        assert np.array_equal(r["y64"][1, 0], r["y64"][1, 1])
+
