@@ -203,6 +203,36 @@ qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int
  *   whole launch.
  */
 #define QLIN_MAX_MULTI 8
+
+/*
+ * Expert bank (MoE) [MOE]: y[m][j][:] = expert ids[m][j] applied to the
+ * quantised activation of token m.  "Comfy Quantization Formats", section
+ * "Embeddings and MoE": a grouped W4A8 / W6A8 bank stores its experts with
+ * the expert and output rows flattened to E * N, and an optional [E, N] bias.
+ *   bank   : device, the bank repacked as one weight of E * N rows
+ *            (qlin_repack with N = E * N), 16-byte aligned.
+ *   E, N   : experts (1..4096) and rows per expert (a multiple of 128 here,
+ *            so that every expert starts on a stream tile).  G >= 32 here.
+ *   ids    : device int32 [M, topk], topk in 1..8: the expert of each token
+ *            and slot.  It may be written by the previous kernel in the
+ *            stream: it is read after the dependency wait.  An id outside
+ *            [0, E) routes nowhere and its output row is not written; a token
+ *            may name one expert in several slots.
+ *   bias   : device fp32 [E, N], or NULL.
+ *   y      : device fp32 [M, topk, N] row-major; every routed (m, j) row is
+ *            fully overwritten.  No routing weights are applied.
+ *   Other arguments, numerics and errors as qlin_forward.  One launch is
+ *   sized for min(E, M * topk) experts; the experts actually routed take its
+ *   row blocks in increasing id order, the remaining blocks return at once.
+ *   Under QLIN_FLAG_PDL the weights are not streamed before the previous
+ *   kernel completes (the routing decides which weights).
+ */
+#define QLIN_MOE_MAX_E 4096
+#define QLIN_MOE_MAX_TOPK 8
+qlin_status qlin_forward_moe(int fmt, int prologue, int M, int E, int64_t N, int64_t K, int64_t G, const void* bank,
+                             const int32_t* ids, int topk, const void* x, const void* gate, const void* up,
+                             const float* gamma, float eps, const float* bias, float* y, void* ws, size_t ws_bytes,
+                             unsigned flags, void* stream);
 qlin_status qlin_forward_multi(int fmt, int prologue, int M, int n, const int64_t* N, int64_t K, int64_t G,
                                const void* const* packed, const void* x, const void* gate, const void* up,
                                const float* gamma, float eps, float* const* y, const float* const* bias, void* ws,

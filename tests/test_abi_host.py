@@ -164,3 +164,27 @@ def test_forward_multi_rejects_bad_arguments(L):
     assert call(Ns=(0, 0)) == qlin.OK                           # nothing to do
     assert call(Ns=(0, 256), packed=(0, 512), ys=(0, 512), ws=None) == qlin.ERR_INVALID_ARG
 
+
+def test_forward_moe_rejects_bad_arguments(L):
+    def call(M=2, E=4, N=256, K=256, G=32, bank=256, ids=256, topk=2, x=256, bias=None, y=256, ws=256, flags=0):
+        return L.qlin_forward_moe(0, 0, M, E, N, K, G, bank, ids, topk, x, None, None, None, 1e-6, bias, y, ws,
+                                  1 << 20, flags, None)
+
+    assert call(E=0) == qlin.ERR_INVALID_ARG
+    assert call(E=4097) == qlin.ERR_INVALID_ARG
+    assert call(topk=0) == qlin.ERR_INVALID_ARG
+    assert call(topk=9) == qlin.ERR_INVALID_ARG
+    assert call(N=16) == qlin.ERR_UNSUPPORTED            # experts must start on a 128-row tile
+    assert call(G=16) == qlin.ERR_UNSUPPORTED            # expert banks: groups of 32 and more
+    assert call(N=24) == qlin.ERR_UNSUPPORTED            # E * N % 16
+    assert call(M=9) == qlin.ERR_UNSUPPORTED
+    assert call(ids=None) == qlin.ERR_INVALID_ARG
+    assert call(ids=258) == qlin.ERR_INVALID_ARG
+    assert call(bank=8) == qlin.ERR_INVALID_ARG
+    assert call(y=None) == qlin.ERR_INVALID_ARG
+    assert call(bias=2) == qlin.ERR_INVALID_ARG
+    assert call(ws=None) == qlin.ERR_INVALID_ARG
+    assert call(flags=2) == qlin.ERR_INVALID_ARG
+    assert call(M=0) == qlin.OK
+    assert call(N=0) == qlin.OK
+

@@ -7,6 +7,7 @@
 // (except the status read-back).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -22,7 +23,8 @@ using namespace qlin;
 namespace {
 
 constexpr int64_t SMEM_TWO_PER_SM = 110 * 1024;  // dynamic bytes that leave room for a second CTA per SM
-constexpr int64_t SMEM_MAX = 225 * 1024;         // dynamic bytes of a CTA alone on its SM
+constexpr int64_t SMEM_MAX = 220 * 1024;         // dynamic bytes of a CTA alone on its SM (static shared
+                                                 // memory and the per-CTA reservation share the 227 KB)
 
 struct DevCache {
   bool init = false;
@@ -41,33 +43,42 @@ qlin_status cuda_status(cudaError_t e) {
   return QLIN_ERR_CUDA;
 }
 
-template <int BITS, int KIND, int G>
+template <int BITS, int KIND, int G, bool MOE>
 const void* fwd_fn() {
-  return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, KIND, G>);
+  return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, KIND, G, MOE>);
 }
-template <int BITS, int KIND>
+// Kernels by group size index: 32, 64, 128, 256, 16, 8, 4.  Expert banks are
+// built for G >= 32; groups of 8 and 4 exist for 4-bit codes only.
+template <int BITS, int KIND, bool MOE>
 const void* fwd_fn_g(int gi) {
   switch (gi) {
-    case 0: return fwd_fn<BITS, KIND, 32>();
-    case 1: return fwd_fn<BITS, KIND, 64>();
-    case 2: return fwd_fn<BITS, KIND, 128>();
-    case 3: return fwd_fn<BITS, KIND, 256>();
-    case 4: return fwd_fn<BITS, KIND, 16>();
+    case 0: return fwd_fn<BITS, KIND, 32, MOE>();
+    case 1: return fwd_fn<BITS, KIND, 64, MOE>();
+    case 2: return fwd_fn<BITS, KIND, 128, MOE>();
+    case 3: return fwd_fn<BITS, KIND, 256, MOE>();
     default: break;
   }
-  if constexpr (BITS == 4) {  // groups of 8 and 4 exist for 4-bit codes only
-    if (gi == 5) return fwd_fn<BITS, KIND, 8>();
-    return fwd_fn<BITS, KIND, 4>();
+  if constexpr (!MOE) {
+    if (gi == 4) return fwd_fn<BITS, KIND, 16, false>();
+    if constexpr (BITS == 4) {
+      if (gi == 5) return fwd_fn<BITS, KIND, 8, false>();
+      return fwd_fn<BITS, KIND, 4, false>();
+    }
   }
   return nullptr;
 }
 int g_index(int64_t G) {
   return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : G == 256 ? 3 : G == 16 ? 4 : G == 8 ? 5 : 6;
 }
-const void* forward_fn(int bits, int kind, int64_t G) {
+template <bool MOE>
+const void* forward_fn_t(int bits, int kind, int64_t G) {
   const int gi = g_index(G);
-  if (bits == 6) return kind == 0 ? fwd_fn_g<6, 0>(gi) : kind == 1 ? fwd_fn_g<6, 1>(gi) : fwd_fn_g<6, 2>(gi);
-  return kind == 0 ? fwd_fn_g<4, 0>(gi) : kind == 1 ? fwd_fn_g<4, 1>(gi) : fwd_fn_g<4, 2>(gi);
+  if (bits == 6)
+    return kind == 0 ? fwd_fn_g<6, 0, MOE>(gi) : kind == 1 ? fwd_fn_g<6, 1, MOE>(gi) : fwd_fn_g<6, 2, MOE>(gi);
+  return kind == 0 ? fwd_fn_g<4, 0, MOE>(gi) : kind == 1 ? fwd_fn_g<4, 1, MOE>(gi) : fwd_fn_g<4, 2, MOE>(gi);
+}
+const void* forward_fn(int bits, int kind, int64_t G, bool moe = false) {
+  return moe ? forward_fn_t<true>(bits, kind, G) : forward_fn_t<false>(bits, kind, G);
 }
 
 // Per-device set-up: SM count, and the kernel attributes every launch relies on
@@ -83,14 +94,15 @@ qlin_status device_cache(DevCache** out) {
     if (e != cudaSuccess) return cuda_status(e);
     for (int bits : {4, 6})
       for (int kind = 0; kind < 3; kind++)
-        for (int64_t G : {4, 8, 16, 32, 64, 128, 256}) {
-          const void* fn = forward_fn(bits, kind, G);
-          if (!fn) continue;
-          e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
-          if (e != cudaSuccess) return cuda_status(e);
-          e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-          if (e != cudaSuccess) return cuda_status(e);
-        }
+        for (int64_t G : {4, 8, 16, 32, 64, 128, 256})
+          for (bool moe : {false, true}) {
+            const void* fn = forward_fn(bits, kind, G, moe);
+            if (!fn) continue;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
+            if (e != cudaSuccess) return cuda_status(e);
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return cuda_status(e);
+          }
     c.init = true;
   }
   *out = &c;
@@ -156,12 +168,12 @@ int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
 // clusters the device holds at once give the waves of the launch; the cost is
 // waves x stream units of the busiest CTA.  The cheapest C wins, ties going
 // to the smaller cluster.  Caller holds g_mu.
-qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int kind, Plan* out) {
+qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int kind, bool moe, Plan* out) {
   const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
   const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
   const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
   if (cmin > cmax) return QLIN_ERR_UNSUPPORTED;
-  const void* fn = forward_fn(g.bits, kind, g.G);
+  const void* fn = forward_fn(g.bits, kind, g.G, moe);
   bool found = false;
   int64_t best_cost = 0;
   for (int64_t c = cmin; c <= cmax; c++) {
@@ -247,6 +259,52 @@ struct Outputs {  // test exports of a single-weight call
 
 // One launch over n weights that share the format, K, G and the activation
 // input: argument checks, the plan, the parameter block, the launch.
+// The plan, the shared part of the parameter block and the launch.  p holds
+// the weights (table or expert bank) already; NB is the launch's row blocks.
+qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, int64_t G, int64_t NB,
+                            const void* x, const void* gate, const void* up, const float* gamma, float eps,
+                            const Outputs& out, void* ws, unsigned flags, void* stream, int64_t fault_unit) {
+  const Geo g = make_geo(fmt, 0, K, G);  // the K geometry every weight shares
+  Plan pl;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevCache* dc = nullptr;
+    qlin_status st = device_cache(&dc);
+    if (st != QLIN_OK) return st;
+    st = make_plan(g, NB, bblock_bytes(g.KB, G, M), *dc, kind, p.moe != 0, &pl);
+    if (st != QLIN_OK) return st;
+  }
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.gate = static_cast<const __nv_bfloat16*>(gate);
+  p.up = static_cast<const __nv_bfloat16*>(up);
+  p.gamma = gamma;
+  p.eps = eps;
+  p.status = static_cast<uint32_t*>(ws);
+  p.acc_out = out.acc;
+  p.q_out = out.q;
+  p.s_out = out.s;
+  p.M = M;
+  p.K = K;
+  p.inv_k = 1.0f / (float)K;
+  p.J = g.J;
+  p.tile_full = g.tile_full;
+  p.unit_full = g.unit_full;
+  p.bpm = (int)bpair_bytes(M);
+  p.bbf = (int)bblock_bytes(g.KB, G, M);
+  p.stage_bytes = pl.stage_bytes;
+  p.b_off = pl.b_off;
+  p.red_off = pl.red_off;
+  p.stages = pl.stages;
+  p.fault_unit = fault_unit;
+  p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
+  void* args[] = {&p};
+  return launch(forward_fn(g.bits, kind, G, p.moe != 0), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
+                dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args, pl.C,
+                (flags & QLIN_FLAG_PDL) != 0);
+}
+
+// One launch over n weights that share the format, K, G and the activation
+// input: argument checks, then the weight table.
 qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int64_t K, int64_t G,
                          const void* const* packed, const void* x, const void* gate, const void* up,
                          const float* gamma, float eps, float* const* ys, const float* const* biases,
@@ -274,16 +332,6 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
   if ((out.acc && !aligned(out.acc, 4)) || (out.s && !aligned(out.s, 4))) return QLIN_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return QLIN_ERR_INVALID_ARG;
   if (ws_bytes < (size_t)WS_HEADER) return QLIN_ERR_WORKSPACE;
-  const Geo g = make_geo(fmt, 0, K, G);  // the K geometry every weight shares
-  Plan pl;
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    DevCache* dc = nullptr;
-    st = device_cache(&dc);
-    if (st != QLIN_OK) return st;
-    st = make_plan(g, NB, bblock_bytes(g.KB, G, M), *dc, kind, &pl);
-    if (st != QLIN_OK) return st;
-  }
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   int nl = 0;
@@ -298,33 +346,41 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
     nl++;
   }
   p.n_lin = nl;
-  p.x = static_cast<const __nv_bfloat16*>(x);
-  p.gate = static_cast<const __nv_bfloat16*>(gate);
-  p.up = static_cast<const __nv_bfloat16*>(up);
-  p.gamma = gamma;
-  p.eps = eps;
-  p.status = static_cast<uint32_t*>(ws);
-  p.acc_out = out.acc;
-  p.q_out = out.q;
-  p.s_out = out.s;
-  p.M = M;
-  p.K = K;
-  p.inv_k = 1.0f / (float)K;
-  p.J = g.J;
-  p.tile_full = g.tile_full;
-  p.unit_full = g.unit_full;
-  p.bpm = (int)bpair_bytes(M);
-  p.bbf = (int)bblock_bytes(g.KB, G, M);
-  p.stage_bytes = pl.stage_bytes;
-  p.b_off = pl.b_off;
-  p.red_off = pl.red_off;
-  p.stages = pl.stages;
-  p.fault_unit = fault_unit;
-  p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
-  void* args[] = {&p};
-  return launch(forward_fn(g.bits, kind, G), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
-                dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args, pl.C,
-                (flags & QLIN_FLAG_PDL) != 0);
+  return plan_and_launch(p, fmt, kind, M, K, G, NB, x, gate, up, gamma, eps, out, ws, flags, stream, fault_unit);
+}
+
+// An expert bank: argument checks, then the routed-expert launch.
+qlin_status moe_impl(int fmt, int kind, int M, int E, int64_t N, int64_t K, int64_t G, const void* bank,
+                     const int32_t* ids, int topk, const void* x, const void* gate, const void* up,
+                     const float* gamma, float eps, const float* bias, float* y, void* ws, size_t ws_bytes,
+                     unsigned flags, void* stream) {
+  if (E < 1 || E > MOE_MAX_E || topk < 1 || topk > MOE_MAX_TOPK || N < 0) return QLIN_ERR_INVALID_ARG;
+  qlin_status st = check_shape_impl(fmt, (int64_t)E * N, K, G);
+  if (st != QLIN_OK) return st;
+  if (N % TILE_N != 0) return QLIN_ERR_UNSUPPORTED;  // every expert starts on a stream tile
+  if (G < 32) return QLIN_ERR_UNSUPPORTED;          // expert banks are built for groups of 32 and more
+  st = check_act(kind, M, x, gate, up, gamma, eps);
+  if (st != QLIN_OK) return st;
+  if (flags & ~QLIN_FLAG_PDL) return QLIN_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return QLIN_OK;
+  if (!bank || !aligned(bank, 16) || !ids || !aligned(ids, 4) || !y || !aligned(y, 4)) return QLIN_ERR_INVALID_ARG;
+  if (bias && !aligned(bias, 4)) return QLIN_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return QLIN_ERR_INVALID_ARG;
+  if (ws_bytes < (size_t)WS_HEADER) return QLIN_ERR_WORKSPACE;
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.moe = 1;
+  p.ids = ids;
+  p.topk = topk;
+  p.E = E;
+  p.ne = N;
+  p.nbe = row_blocks(N);
+  p.bank = static_cast<const uint8_t*>(bank);
+  p.bank_bias = bias;
+  p.ymoe = y;
+  const int64_t slots = std::min<int64_t>(E, (int64_t)M * topk);  // routed experts, at most
+  return plan_and_launch(p, fmt, kind, M, K, G, slots * p.nbe, x, gate, up, gamma, eps, Outputs(), ws, flags,
+                         stream, -1);
 }
 
 // ---------------------------------------------------------------------------
@@ -482,6 +538,14 @@ qlin_status qlin_forward_multi(int fmt, int prologue, int M, int n, const int64_
                       ws_bytes, flags, stream, false);
 }
 
+qlin_status qlin_forward_moe(int fmt, int prologue, int M, int E, int64_t N, int64_t K, int64_t G, const void* bank,
+                             const int32_t* ids, int topk, const void* x, const void* gate, const void* up,
+                             const float* gamma, float eps, const float* bias, float* y, void* ws, size_t ws_bytes,
+                             unsigned flags, void* stream) {
+  return moe_impl(fmt, prologue, M, E, N, K, G, bank, ids, topk, x, gate, up, gamma, eps, bias, y, ws, ws_bytes, flags,
+                  stream);
+}
+
 qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, int64_t* ctas, int64_t* units,
                                      int64_t* stream_bytes) {
   qlin_status st = check_shape_impl(fmt, N, K, G);
@@ -494,7 +558,7 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, i
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, row_blocks(N), bblock_bytes(g.KB, G, MAX_M), *dc, QLIN_PROLOGUE_NONE, &pl);
+    st = make_plan(g, row_blocks(N), bblock_bytes(g.KB, G, MAX_M), *dc, QLIN_PROLOGUE_NONE, false, &pl);
     if (st != QLIN_OK) return st;
   }
   *ctas = (int64_t)pl.C * pl.NB;

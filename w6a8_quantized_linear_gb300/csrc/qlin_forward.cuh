@@ -58,6 +58,15 @@ struct FwdParams {
   const float* bias[MAX_LIN]; // fp32 [N[l]] or null
   int64_t N[MAX_LIN], T[MAX_LIN];
   int64_t blk0[MAX_LIN + 1];
+  // Expert bank (moe = 1): the launch's row blocks are those of the routed
+  // experts, a routed-expert slot a owning blocks [a * nbe, (a + 1) * nbe).
+  int moe;
+  const int32_t* ids;         // [M, topk] expert of each token and slot
+  int topk, E;
+  int64_t ne, nbe;            // rows per expert, 256-row blocks per expert
+  const uint8_t* bank;        // repacked [E * ne, K] stream
+  const float* bank_bias;     // [E, ne] or null
+  float* ymoe;                // [M, topk, ne]
   const __nv_bfloat16* x;     // NONE, RMSNORM: [M, K]
   const __nv_bfloat16* gate;  // SWIGLU: [M, K]
   const __nv_bfloat16* up;    // SWIGLU: [M, K]
@@ -258,7 +267,7 @@ __device__ __forceinline__ void group_mma(const uint32_t (&a)[4], const uint32_t
   }
 }
 
-template <int BITS, int KIND, int G>
+template <int BITS, int KIND, int G, bool MOE>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
   // G < 32: groups are narrower than a 32-wide pair; each group is its own
   // chain (one MMA) with its own start value, GPP groups per pair.
@@ -280,6 +289,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   __shared__ float s_red[CONSUMER_WARPS][MAX_M][2];
   __shared__ __align__(16) float s_slot[MAX_CLUSTER][MAX_M][2];  // rank r's (amax, sum x^2) per row
   __shared__ float s_row[MAX_M][2];                               // s, code factor c
+  __shared__ uint32_t s_tokmask[MAX_M];                            // expert bank: slots of each token
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // TMA destinations and vector loads need 16-byte alignment of the dynamic
@@ -307,6 +317,69 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       T = p.T[l];
       blk_first = p.blk0[l];
     }
+  }
+  if constexpr (MOE) {
+    __shared__ uint32_t s_ebits[MOE_MAX_E / 32];  // routed experts
+    __shared__ int s_expert;
+    // Expert bank: the routing comes from an earlier kernel, so nothing is
+    // read before the dependency wait.  The routed experts, in increasing
+    // id, take the row-block slots in order; a slot past the last routed
+    // expert has no work, and its whole cluster (same blockIdx.y) leaves
+    // here, before any barrier or shared-memory exchange.
+    pdl_wait();
+    for (int w = tid; w < MOE_MAX_E / 32; w += GEMV_THREADS) s_ebits[w] = 0u;
+    if (tid == 0) s_expert = -1;
+    __syncthreads();
+    if (tid < p.M * p.topk) {
+      const int e = p.ids[tid];
+      if (e >= 0 && e < p.E) atomicOr(&s_ebits[e >> 5], 1u << (e & 31));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      constexpr int WPL = MOE_MAX_E / 32 / 32;  // bitmap words per lane
+      uint32_t wd[WPL];
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < WPL; i++) {
+        wd[i] = s_ebits[lane * WPL + i];
+        cnt += __popc(wd[i]);
+      }
+      int incl = cnt;  // inclusive prefix of the counts over the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int a = (int)(blockIdx.y / p.nbe);
+      int r = a - (incl - cnt);
+      if (r >= 0 && r < cnt) {
+#pragma unroll
+        for (int i = 0; i < WPL; i++) {
+          const int pc = __popc(wd[i]);
+          if (r >= 0 && r < pc) {
+            uint32_t v = wd[i];
+            for (int k = 0; k < r; k++) v &= v - 1u;  // drop the r lowest set bits
+            s_expert = (lane * WPL + i) * 32 + (__ffs(v) - 1);
+          }
+          r -= pc;
+        }
+      }
+    }
+    __syncthreads();
+    const int expert = s_expert;
+    if (expert < 0) return;
+    if (tid < p.M) {
+      uint32_t mask = 0;
+      for (int j = 0; j < p.topk; j++)
+        if (p.ids[tid * p.topk + j] == expert) mask |= 1u << j;
+      s_tokmask[tid] = mask;
+    }
+    packed = p.bank + (int64_t)expert * (p.ne / TILE_N) * p.tile_full;
+    y = p.ymoe;
+    bias = p.bank_bias ? p.bank_bias + (int64_t)expert * p.ne : nullptr;
+    N = p.ne;
+    T = p.ne / TILE_N;
+    blk_first = (int64_t)(blockIdx.y / p.nbe) * p.nbe;
   }
   const int64_t rb = (int64_t)blockIdx.y - blk_first;
   const int64_t j0 = split_begin(crank, p.J, C), j1 = split_begin(crank + 1, p.J, C);
@@ -736,13 +809,22 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         if (slab * SLAB >= Rt) continue;
         const int64_t n = tt * TILE_N + slab * SLAB + gs;
         const float b0 = bias ? bias[n] : 0.f, b8 = bias ? bias[n + 8] : 0.f;
-        if (2 * ts < M) {
-          y[(int64_t)(2 * ts) * N + n] = __fmaf_rn(sm0, v[4 * a + 0], b0);
-          y[(int64_t)(2 * ts) * N + n + 8] = __fmaf_rn(sm0, v[4 * a + 2], b8);
-        }
-        if (2 * ts + 1 < M) {
-          y[(int64_t)(2 * ts + 1) * N + n] = __fmaf_rn(sm1, v[4 * a + 1], b0);
-          y[(int64_t)(2 * ts + 1) * N + n + 8] = __fmaf_rn(sm1, v[4 * a + 3], b8);
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          const int m = 2 * ts + h;
+          if (m >= M) continue;
+          const float sm = h == 0 ? sm0 : sm1;
+          const float lo = __fmaf_rn(sm, v[4 * a + h], b0), hi = __fmaf_rn(sm, v[4 * a + 2 + h], b8);
+          if constexpr (!MOE) {
+            y[(int64_t)m * N + n] = lo;
+            y[(int64_t)m * N + n + 8] = hi;
+          } else {  // every slot of token m routed to this expert
+            for (uint32_t msk = s_tokmask[m]; msk; msk &= msk - 1u) {
+              const int j = __ffs(msk) - 1;
+              y[((int64_t)m * p.topk + j) * N + n] = lo;
+              y[((int64_t)m * p.topk + j) * N + n + 8] = hi;
+            }
+          }
         }
       }
     }

@@ -24,6 +24,8 @@ constexpr int KSTEP = 16;          // k per bf16 MMA
 constexpr int PAIR_K = 32;         // two k-steps share one plane word pair
 constexpr int MAX_M = 8;           // rows of the activation (N side of the MMA)
 constexpr int MAX_LIN = 8;         // weights sharing one activation in one launch
+constexpr int MOE_MAX_E = 4096;    // experts in one bank
+constexpr int MOE_MAX_TOPK = 8;    // routed experts per token
 constexpr int TILES_PER_CTA = 2;   // a CTA owns a 256-row block: two stream tiles
 constexpr int ROWS_PER_CTA = TILES_PER_CTA * TILE_N;
 constexpr int CONSUMER_WARPS = 8;  // each owns two slabs (32 rows) of the block

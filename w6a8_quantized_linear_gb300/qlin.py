@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
                                       ctypes.c_uint, vp]),
                 "qlin_forward_multi": (st, [i32, i32, i32, i32, vp, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float,
                                             vp, vp, vp, sz, ctypes.c_uint, vp]),
+                "qlin_forward_moe": (st, [i32, i32, i32, i32, i64, i64, i64, vp, vp, i32, vp, vp, vp, vp,
+                                          ctypes.c_float, vp, vp, vp, sz, ctypes.c_uint, vp]),
                 "qlin_forward_launch_info": (st, [i32, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                                   ctypes.POINTER(i64)]),
                 "qlin_read_device_status": (st, [vp, vp]),
@@ -197,6 +199,28 @@ def forward_multi(fmt, prologue, packed: list, N: list, K: int, G: int, x=None, 
                                     float(eps), ctypes.cast(y_arr, ctypes.c_void_p),
                                     None if b_arr is None else ctypes.cast(b_arr, ctypes.c_void_p), _ptr(ws), ws.numel(), flags,
                                     _stream(stream)), "forward_multi")
+    return y
+
+
+def forward_moe(fmt, prologue, bank: torch.Tensor, E: int, N: int, K: int, G: int, ids: torch.Tensor, x=None,
+                gate=None, up=None, gamma=None, eps: float = 1e-6, bias: torch.Tensor | None = None,
+                y: torch.Tensor | None = None, ws: torch.Tensor | None = None, flags: int = 0,
+                stream=None) -> torch.Tensor:
+    """Expert bank: y[m, j] = expert ids[m, j] applied to token m (fp32 [M, topk, N]).
+    ``bank`` is the [E * N, K] bank repacked as one weight; ``ids`` int32 [M, topk]
+    on the device."""
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    topk = ids.shape[1]
+    if ids.dtype != torch.int32 or not ids.is_contiguous():
+        raise ValueError("ids must be a contiguous int32 [M, topk] tensor")
+    if y is None:
+        y = torch.empty(M, topk, N, dtype=torch.float32, device=bank.device)
+    if ws is None:
+        ws = new_workspace(forward_workspace_bytes(fmt, E * N, K, G), bank.device, stream)
+    _check(lib().qlin_forward_moe(_fmt(fmt), _pro(prologue), M, E, N, K, G, _ptr(bank), _ptr(ids), topk, _ptr(x),
+                                  _ptr(gate), _ptr(up), _ptr(gamma), float(eps), _ptr(bias), _ptr(y), _ptr(ws),
+                                  ws.numel(), flags, _stream(stream)), "forward_moe")
     return y
 
 
