@@ -1,8 +1,10 @@
 """Build libqlin.so (sm_103a) in-tree with nvcc.
 
-One translation unit, one -gencode, shared CUDA runtime (so the library and
-PyTorch share one runtime and one notion of the current device).  The output
-goes to ``w6a8_quantized_linear_gb300/_build/libqlin.so`` (git-ignored).
+Four translation units compiled in parallel (the host API with the repack
+kernels, and the forward-kernel variants of each prologue kind), one
+-gencode, shared CUDA runtime (so the library and PyTorch share one runtime
+and one notion of the current device).  The output goes to
+``w6a8_quantized_linear_gb300/_build/libqlin.so`` (git-ignored).
 """
 from __future__ import annotations
 
@@ -16,7 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libqlin.so")
-SOURCES = [os.path.join(CSRC, f) for f in ("qlin_api.cu", "qlin_forward.cuh", "qlin_repack.cuh", "qlin_layout.h", "qlin_ptx.cuh")] + [
+UNITS = ["qlin_api.cu", "qlin_kernels_none.cu", "qlin_kernels_rmsnorm.cu", "qlin_kernels_swiglu.cu"]
+SOURCES = [os.path.join(CSRC, f) for f in UNITS + ["qlin_forward.cuh", "qlin_repack.cuh", "qlin_layout.h",
+                                                   "qlin_ptx.cuh", "qlin_instances.h"]] + [
     os.path.join(INCLUDE, "qlin.h")]
 
 
@@ -43,18 +47,44 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = nvcc_path()
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
-           "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared", "-Xlinker", f"-rpath,{cuda_lib}",
-           "-I", INCLUDE, os.path.join(CSRC, "qlin_api.cu"), "-o", tmp]
+    tag = f".tmp{os.getpid()}"
+    # kernels are instantiated in one unit and launched from another, so their
+    # host stubs need external linkage
+    common = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
+              "-static-global-template-stub=false", "-Xcompiler", "-fPIC", "-I", INCLUDE]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
+        common.insert(1, "-Xptxas=-v")
+    objs, procs = [], []
+    try:
+        return _compile_and_link(nvcc, cuda_lib, common, tag, verbose)
+    finally:
+        for f in os.listdir(BUILD):  # objects of this build, also after a failure
+            if f.endswith(tag + ".o"):
+                os.remove(os.path.join(BUILD, f))
+
+
+def _compile_and_link(nvcc, cuda_lib, common, tag, verbose):
+    objs, procs = [], []
+    for u in UNITS:
+        obj = os.path.join(BUILD, u.replace(".cu", tag + ".o"))
+        cmd = common + ["-c", os.path.join(CSRC, u), "-o", obj]
+        procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
+        objs.append(obj)
+    logs = []
+    for cmd, pr in procs:
+        out, _ = pr.communicate()
+        logs.append(out)
+        if pr.returncode != 0:
+            raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + out)
+    tmp = LIB + tag
+    cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-cudart", "shared", "-Xlinker",
+           f"-rpath,{cuda_lib}"] + objs + ["-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+        raise RuntimeError("nvcc link failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
     os.replace(tmp, LIB)
     if verbose:
-        print(r.stdout + r.stderr)
+        print("".join(logs) + r.stdout + r.stderr)
     return LIB
 
 

@@ -16,7 +16,13 @@
 
 #include "qlin.h"
 #include "qlin_forward.cuh"
+#include "qlin_instances.h"
 #include "qlin_repack.cuh"
+
+// the forward kernels live in qlin_kernels_{none,rmsnorm,swiglu}.cu
+QLIN_KERNELS_OF_KIND(QLIN_DECLARE_EXTERN, 0)
+QLIN_KERNELS_OF_KIND(QLIN_DECLARE_EXTERN, 1)
+QLIN_KERNELS_OF_KIND(QLIN_DECLARE_EXTERN, 2)
 
 using namespace qlin;
 

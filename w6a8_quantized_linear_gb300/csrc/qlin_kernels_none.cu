@@ -1,0 +1,5 @@
+// Forward-kernel variants with the none prologue (see qlin_instances.h).
+#include "qlin_forward.cuh"
+#include "qlin_instances.h"
+
+QLIN_KERNELS_OF_KIND(QLIN_INSTANTIATE, 0)
