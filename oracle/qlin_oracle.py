@@ -66,7 +66,7 @@ import numpy as np
 __all__ = [
     "BITS", "code_offset", "file_code_bytes", "file_scale_bytes", "file_bytes",
     "unpack_file", "pack_file", "bf16_bits_to_f64", "prologue", "quantize_rows",
-    "group_acc", "forward", "forward_moe", "STREAM_TN", "stream_kb", "unpack_stream",
+    "group_acc", "group_acc_codebook", "forward", "forward_moe", "STREAM_TN", "stream_kb", "unpack_stream",
 ]
 
 BITS = {"w4a8": 4, "w6a8": 6}
@@ -239,15 +239,34 @@ def group_acc(q, codes, fmt: str, G: int) -> np.ndarray:
     return acc_i.transpose(1, 2, 0)                                      # [M, N, g]
 
 
+def group_acc_codebook(q, codes, codebook, G: int) -> np.ndarray:
+    """acc[m, n, g] = sum_{k in group g} q[m, k] * codebook[codes[n, k]], float64.
+
+    "Comfy Quantization Formats", section "Format options": an asym_w4a8_int8
+    weight may store a float [16] weight_codebook that replaces the uniform
+    levels (code - 8).  Reading: the level of code c is codebook[c] (fp32),
+    one table per weight; the sums are no longer integers."""
+    q = np.asarray(q, dtype=np.float64)
+    L = np.asarray(codebook, dtype=np.float32).astype(np.float64)[np.asarray(codes)]
+    M, K = q.shape
+    N = L.shape[0]
+    ng = K // G
+    qg = q.reshape(M, ng, G).transpose(1, 0, 2)                          # [g, M, G]
+    Lg = L.reshape(N, ng, G).transpose(1, 2, 0)                          # [g, G, N]
+    return np.matmul(qg, Lg).transpose(1, 2, 0)                          # [M, N, g]
+
+
 # ----------------------------------------------------------------------------
 # 5. the whole path
 # ----------------------------------------------------------------------------
 
 def forward(fmt: str, kind: str, N: int, K: int, G: int, buf, x=None, gate=None, up=None,
-            gamma=None, eps: float = 1e-6, cols=None, stream: bool = False, bias=None) -> dict:
+            gamma=None, eps: float = 1e-6, cols=None, stream: bool = False, bias=None, codebook=None) -> dict:
     """y[M, N] = s_m * sum_g sw[n, g] * acc[m, n, g] (+ bias[n]), in float64,
     rounded to fp32.  ``bias`` is an optional fp32 [N] vector (reading: an
-    ordinary float bias is added after the scaled product).
+    ordinary float bias is added after the scaled product).  ``codebook`` is
+    an optional fp32 [16] table of levels for 4-bit codes (``acc`` is then
+    float64 rather than integer).
 
     ``buf`` is the checkpoint layout (or, with ``stream=True``, the repacked
     stream layout).  ``cols`` restricts the computation to the listed output
@@ -262,7 +281,11 @@ def forward(fmt: str, kind: str, N: int, K: int, G: int, buf, x=None, gate=None,
         codes, sw = unpack_file(fmt, N, K, G, buf, rows=cols)
     a = prologue(kind, x=x, gate=gate, up=up, gamma=gamma, eps=eps)
     q, s, v = quantize_rows(a, fp32=(kind == "none"))
-    acc = group_acc(q, codes, fmt, G)
+    if codebook is not None:
+        assert fmt == "w4a8", "only 4-bit codes have a codebook"
+        acc = group_acc_codebook(q, codes, codebook, G)
+    else:
+        acc = group_acc(q, codes, fmt, G)
     y64 = s[:, None] * (acc.astype(np.float64) * sw.astype(np.float64)[None, :, :]).sum(axis=2)
     if bias is not None:
         b = np.asarray(bias, dtype=np.float32).astype(np.float64)

@@ -79,8 +79,9 @@ def _bitstream_codes(fmt, N, K, wbuf):
     return out
 
 
-def _bruteforce_y(fmt, N, K, G, wbuf, q, s):
-    """y from raw bytes by pure-Python loops over the dequantised weight."""
+def _bruteforce_y(fmt, N, K, G, wbuf, q, s, codebook=None):
+    """y from raw bytes by pure-Python loops over the dequantised weight (levels
+    code - offset, or codebook[code])."""
     b = {"w4a8": 4, "w6a8": 6}[fmt]
     codes = _bitstream_codes(fmt, N, K, wbuf)
     off = N * K * b // 8
@@ -93,7 +94,8 @@ def _bruteforce_y(fmt, N, K, G, wbuf, q, s):
         for n in range(N):
             tot = 0.0
             for k in range(K):
-                w = sw[n][k // G] * float(int(codes[n, k]) - (1 << (b - 1)))
+                lv = float(codebook[int(codes[n, k])]) if codebook is not None else float(int(codes[n, k]) - (1 << (b - 1)))
+                w = sw[n][k // G] * lv
                 tot += (s[m] * float(q[m, k])) * w
             y[m, n] = tot
     return y
@@ -345,4 +347,23 @@ def check_moe(O, seed=10):
                 one = O.forward(fmt, "rmsnorm", N, K, G, own, x=bits_of(x[m:m + 1]), gamma=gamma, bias=bias[e])
                 assert np.array_equal(r["y64"][m, j], one["y64"][0]), (fmt, m, j)
         assert np.array_equal(r["y64"][1, 0], r["y64"][1, 1])
+
+
+def check_codebook(O, seed=11):
+    """A 4-bit codebook replaces the uniform levels: the uniform table
+    (c - 8) gives back the plain result exactly, and any table matches the
+    brute-force dequantised product."""
+    rng = np.random.default_rng(seed)
+    N, K, G = 16, 64, 32
+    codes = rng.integers(0, 16, (N, K))
+    sw = rng.uniform(0.01, 0.02, (N, K // G)).astype(np.float32)
+    wbuf = O.pack_file("w4a8", codes, sw)
+    x = torch.randn(3, K, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+    plain = O.forward("w4a8", "none", N, K, G, wbuf, x=bits_of(x))
+    uni = O.forward("w4a8", "none", N, K, G, wbuf, x=bits_of(x), codebook=np.arange(16, dtype=np.float32) - 8)
+    assert np.array_equal(plain["y64"], uni["y64"])
+    cb = np.sort(rng.normal(size=16)).astype(np.float32)  # an NF4-like, non-uniform table
+    r = O.forward("w4a8", "rmsnorm", N, K, G, wbuf, x=bits_of(x), gamma=np.ones(K, np.float32), codebook=cb)
+    yb = _bruteforce_y("w4a8", N, K, G, wbuf, r["q"], r["s"], codebook=cb)
+    assert np.allclose(r["y64"], yb, rtol=1e-12, atol=1e-12 * np.abs(yb).max())
 

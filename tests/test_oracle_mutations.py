@@ -34,12 +34,13 @@ MUTANTS = {
     "stream_scale_pairs_transposed": ("f.transpose(1, 3, 2, 0)", "f.transpose(1, 2, 3, 0)"),
     "bias_dropped": ("y64 = y64 + (b if cols is None", "y64 = y64 + 0 * (b if cols is None"),
     "moe_expert_rows_offset": ("cols = e * N + sel", "cols = e * N + sel + (N if e == 0 else 0)"),
+    "codebook_index_flipped": ("astype(np.float64)[np.asarray(codes)]", "astype(np.float64)[np.asarray(codes) ^ 8]"),
     "bias_scaled_by_row_scale": ("y64 = y64 + (b if cols is None else b[np.asarray(cols)])[None, :]",
                                  "y64 = y64 + s[:, None] * (b if cols is None else b[np.asarray(cols)])[None, :]"),
 }
 
 PINS = ["hand_example", "file_layout", "forward_bruteforce", "quantize", "prologues",
-        "closed_forms", "invariants", "stream_positions", "stream_bijection", "bias", "moe"]
+        "closed_forms", "invariants", "stream_positions", "stream_bijection", "bias", "moe", "codebook"]
 
 
 def build_mutant(old, new):
