@@ -270,6 +270,64 @@ class Stack:
         return g, n, nbytes
 
 
+def next_rows(stack, stream, iters: int, peak: float):
+    """The widened paths on the stack's gate weights (17408 x 5120, G = 128,
+    RMSNorm prologue), 64 launches on 64 distinct weights in one graph each:
+    the single-weight launch, the same weights with a 16-level codebook, and
+    each weight read as an expert bank of 17 experts x 1024 rows (8 routed
+    experts for one token; 2 per token for 8 tokens)."""
+    import torch
+
+    from w6a8_quantized_linear_gb300 import qlin
+    K, N = stack.shape["gate"]
+    G = stack.G
+    gen = torch.Generator().manual_seed(5)
+    x1 = torch.randn(1, K, generator=gen).to(torch.bfloat16).to(stack.dev)
+    x8 = torch.randn(8, K, generator=gen).to(torch.bfloat16).to(stack.dev)
+    gamma = torch.rand(K, generator=gen).add(0.5).to(stack.dev)
+    cb = torch.sort(torch.randn(16, generator=gen)).values.to(stack.dev)
+    E, NE = 17, 1024
+    ids1 = torch.randperm(E, generator=gen)[:8].view(1, 8).to(torch.int32).to(stack.dev)
+    ids8 = torch.stack([torch.randperm(E, generator=gen)[:2] for _ in range(8)]).to(torch.int32).to(stack.dev)
+    weights = [row["gate"] for row in stack.weights]
+    y = torch.empty(8 * N, device=stack.dev)
+    wbytes = qlin.packed_bytes("w4a8", N, K, G)
+
+    def plain(w):
+        qlin.forward("w4a8", "rmsnorm", w, N, K, G, x=x1, gamma=gamma, y=y[:N].view(1, N), ws=stack.ws,
+                     flags=qlin.FLAG_PDL, stream=stream)
+
+    def codebook(w):
+        qlin.forward_codebook("w4a8", "rmsnorm", w, cb, N, K, G, x=x1, gamma=gamma, y=y[:N].view(1, N),
+                              ws=stack.ws, flags=qlin.FLAG_PDL, stream=stream)
+
+    def moe(ids, x):
+        def f(w):
+            qlin.forward_moe("w4a8", "rmsnorm", w, E, NE, K, G, ids, x=x, gamma=gamma,
+                             y=y[:ids.numel() * NE].view(ids.shape[0], ids.shape[1], NE), ws=stack.ws,
+                             flags=qlin.FLAG_PDL, stream=stream)
+        return f
+
+    cases = [("single_weight", plain, wbytes), ("codebook", codebook, wbytes),
+             ("moe_m1_top8", moe(ids1, x1), wbytes * 8 // E), ("moe_m8_top2", moe(ids8, x8),
+                                                                wbytes * len(set(ids8.flatten().tolist())) // E)]
+    out = {}
+    for name, f, nbytes in cases:
+        f(weights[0])
+        torch.cuda.synchronize(stack.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for w in weights:
+                    f(w)
+        t = time_graph(g, stream, iters, 3)
+        us = t * 1e3 / len(weights)
+        out[name] = {"us_per_launch": us, "weight_bytes_per_launch": nbytes, "GB/s": nbytes / (us * 1e-6) / 1e9,
+                     "frac_of_measured_hbm": nbytes / (us * 1e-6) / 1e9 / peak}
+        del g
+    return out
+
+
 def time_graph(g, stream, iters: int, warmup: int, ws_world=1, device=None):
     import torch
     for _ in range(warmup):
@@ -457,6 +515,8 @@ def main():
             e["bytes_per_launch"] = nbytes // n
             del g
 
+    widened = next_rows(stack, stream, max(3, args.steps // 2), peak)
+
     # end to end through the public call with host buffers: pinned host
     # activations in, every call's output back, each step
     d_act = stack.act[:stack.act_per_row]   # the M = 1 step's inputs
@@ -515,6 +575,7 @@ def main():
         "separate_launches": {"launches_per_step": ncalls_sep, "value": world * wb / (ts1 * 1e-3) / 1e9,
                               "ms_per_step": ts1, "m8": world * wb / (ts8 * 1e-3) / 1e9, "t8_over_t1": ts8 / ts1},
         "per_group": per,
+        "widened_paths": widened,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic["bytes_per_launch"] if traffic else None,
                      "kernel": "qlin_forward_kernel<4,1,128>: the gate/up multi-weight launch, M=1, "

@@ -233,6 +233,28 @@ qlin_status qlin_forward_moe(int fmt, int prologue, int M, int E, int64_t N, int
                              const int32_t* ids, int topk, const void* x, const void* gate, const void* up,
                              const float* gamma, float eps, const float* bias, float* y, void* ws, size_t ws_bytes,
                              unsigned flags, void* stream);
+/*
+ * 4-bit codes with a codebook [FMT]: "Comfy Quantization Formats", section
+ * "Format options" -- a W4A8 weight may carry a float [16] codebook that
+ * replaces the uniform levels (code - 8); W6A8 has none.  Here the level of
+ * code c is codebook[c], scaled per group by the weight scale as usual:
+ *   y[m][n] = s_m * sum_g sw[n][g] * sum_{k in g} q[m][k] * codebook[code[n][k]]
+ *             (+ bias[n]).
+ *   fmt      : QLIN_W4A8 only (else QLIN_ERR_INVALID_ARG); G >= 32 here.
+ *   packed   : the repacked stream, as for qlin_forward (same repack).
+ *   codebook : device fp32 [16], 4-byte aligned.  It is read like `packed`
+ *              (before the dependency wait under QLIN_FLAG_PDL).
+ *   bias     : device fp32 [N], or NULL.
+ *   Other arguments, numerics and errors as qlin_forward, except that the
+ *   group sums are not exact integers: the table is scaled by the power of
+ *   two that puts its largest magnitude in [2^14, 2^15) and rounded to fp16
+ *   (11 significant bits, relative error <= 2^-12 per level), products and
+ *   sums in fp32, the power of two removed exactly afterwards.
+ */
+qlin_status qlin_forward_codebook(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G, const void* packed,
+                                  const float* codebook, const void* x, const void* gate, const void* up,
+                                  const float* gamma, float eps, const float* bias, float* y, void* ws,
+                                  size_t ws_bytes, unsigned flags, void* stream);
 qlin_status qlin_forward_multi(int fmt, int prologue, int M, int n, const int64_t* N, int64_t K, int64_t G,
                                const void* const* packed, const void* x, const void* gate, const void* up,
                                const float* gamma, float eps, float* const* y, const float* const* bias, void* ws,

@@ -188,3 +188,25 @@ def test_forward_moe_rejects_bad_arguments(L):
     assert call(M=0) == qlin.OK
     assert call(N=0) == qlin.OK
 
+
+
+def test_forward_codebook_rejects_bad_arguments(L):
+    def call(fmt=0, M=2, N=256, K=256, G=32, packed=256, cb=256, x=256, bias=None, y=256, ws=256, flags=0):
+        return L.qlin_forward_codebook(fmt, 0, M, N, K, G, packed, cb, x, None, None, None, 1e-6, bias, y, ws,
+                                       1 << 20, flags, None)
+
+    assert call(fmt=1) == qlin.ERR_INVALID_ARG           # 6-bit codes have no codebook
+    assert call(cb=None) == qlin.ERR_INVALID_ARG
+    assert call(cb=258) == qlin.ERR_INVALID_ARG          # misaligned table
+    assert call(G=16, K=256) == qlin.ERR_UNSUPPORTED     # codebooks: groups of 32 and more
+    assert call(G=8) == qlin.ERR_UNSUPPORTED
+    assert call(K=48, G=16) == qlin.ERR_UNSUPPORTED
+    assert call(N=24) == qlin.ERR_UNSUPPORTED
+    assert call(M=9) == qlin.ERR_UNSUPPORTED
+    assert call(packed=8) == qlin.ERR_INVALID_ARG
+    assert call(bias=2) == qlin.ERR_INVALID_ARG
+    assert call(y=None) == qlin.ERR_INVALID_ARG
+    assert call(ws=None) == qlin.ERR_INVALID_ARG
+    assert call(flags=2) == qlin.ERR_INVALID_ARG
+    assert call(M=0) == qlin.OK
+    assert call(N=0) == qlin.OK

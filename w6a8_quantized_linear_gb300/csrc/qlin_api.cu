@@ -49,42 +49,47 @@ qlin_status cuda_status(cudaError_t e) {
   return QLIN_ERR_CUDA;
 }
 
-template <int BITS, int KIND, int G, bool MOE>
+template <int BITS, int KIND, int G, int MODE>
 const void* fwd_fn() {
-  return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, KIND, G, MOE>);
+  return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, KIND, G, MODE>);
 }
-// Kernels by group size index: 32, 64, 128, 256, 16, 8, 4.  Expert banks are
-// built for G >= 32; groups of 8 and 4 exist for 4-bit codes only.
-template <int BITS, int KIND, bool MOE>
+// Kernels by group size index: 32, 64, 128, 256, 16, 8, 4.  Expert banks
+// (mode 1) and codebooks (mode 2, 4-bit codes) are built for G >= 32; groups
+// of 8 and 4 exist for 4-bit codes only.
+template <int BITS, int KIND, int MODE>
 const void* fwd_fn_g(int gi) {
-  switch (gi) {
-    case 0: return fwd_fn<BITS, KIND, 32, MOE>();
-    case 1: return fwd_fn<BITS, KIND, 64, MOE>();
-    case 2: return fwd_fn<BITS, KIND, 128, MOE>();
-    case 3: return fwd_fn<BITS, KIND, 256, MOE>();
-    default: break;
-  }
-  if constexpr (!MOE) {
-    if (gi == 4) return fwd_fn<BITS, KIND, 16, false>();
-    if constexpr (BITS == 4) {
-      if (gi == 5) return fwd_fn<BITS, KIND, 8, false>();
-      return fwd_fn<BITS, KIND, 4, false>();
+  if constexpr (MODE == 2 && BITS != 4) return nullptr;
+  else {
+    switch (gi) {
+      case 0: return fwd_fn<BITS, KIND, 32, MODE>();
+      case 1: return fwd_fn<BITS, KIND, 64, MODE>();
+      case 2: return fwd_fn<BITS, KIND, 128, MODE>();
+      case 3: return fwd_fn<BITS, KIND, 256, MODE>();
+      default: break;
     }
+    if constexpr (MODE == 0) {
+      if (gi == 4) return fwd_fn<BITS, KIND, 16, 0>();
+      if constexpr (BITS == 4) {
+        if (gi == 5) return fwd_fn<BITS, KIND, 8, 0>();
+        return fwd_fn<BITS, KIND, 4, 0>();
+      }
+    }
+    return nullptr;
   }
-  return nullptr;
 }
 int g_index(int64_t G) {
   return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : G == 256 ? 3 : G == 16 ? 4 : G == 8 ? 5 : 6;
 }
-template <bool MOE>
+template <int MODE>
 const void* forward_fn_t(int bits, int kind, int64_t G) {
   const int gi = g_index(G);
   if (bits == 6)
-    return kind == 0 ? fwd_fn_g<6, 0, MOE>(gi) : kind == 1 ? fwd_fn_g<6, 1, MOE>(gi) : fwd_fn_g<6, 2, MOE>(gi);
-  return kind == 0 ? fwd_fn_g<4, 0, MOE>(gi) : kind == 1 ? fwd_fn_g<4, 1, MOE>(gi) : fwd_fn_g<4, 2, MOE>(gi);
+    return kind == 0 ? fwd_fn_g<6, 0, MODE>(gi) : kind == 1 ? fwd_fn_g<6, 1, MODE>(gi) : fwd_fn_g<6, 2, MODE>(gi);
+  return kind == 0 ? fwd_fn_g<4, 0, MODE>(gi) : kind == 1 ? fwd_fn_g<4, 1, MODE>(gi) : fwd_fn_g<4, 2, MODE>(gi);
 }
-const void* forward_fn(int bits, int kind, int64_t G, bool moe = false) {
-  return moe ? forward_fn_t<true>(bits, kind, G) : forward_fn_t<false>(bits, kind, G);
+const void* forward_fn(int bits, int kind, int64_t G, int mode = 0) {
+  return mode == 1 ? forward_fn_t<1>(bits, kind, G) : mode == 2 ? forward_fn_t<2>(bits, kind, G)
+                                                                : forward_fn_t<0>(bits, kind, G);
 }
 
 // Per-device set-up: SM count, and the kernel attributes every launch relies on
@@ -101,8 +106,8 @@ qlin_status device_cache(DevCache** out) {
     for (int bits : {4, 6})
       for (int kind = 0; kind < 3; kind++)
         for (int64_t G : {4, 8, 16, 32, 64, 128, 256})
-          for (bool moe : {false, true}) {
-            const void* fn = forward_fn(bits, kind, G, moe);
+          for (int mode = 0; mode < 3; mode++) {
+            const void* fn = forward_fn(bits, kind, G, mode);
             if (!fn) continue;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
             if (e != cudaSuccess) return cuda_status(e);
@@ -174,12 +179,12 @@ int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
 // clusters the device holds at once give the waves of the launch; the cost is
 // waves x stream units of the busiest CTA.  The cheapest C wins, ties going
 // to the smaller cluster.  Caller holds g_mu.
-qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int kind, bool moe, Plan* out) {
+qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int kind, int mode, Plan* out) {
   const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
   const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
   const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
   if (cmin > cmax) return QLIN_ERR_UNSUPPORTED;
-  const void* fn = forward_fn(g.bits, kind, g.G, moe);
+  const void* fn = forward_fn(g.bits, kind, g.G, mode);
   bool found = false;
   int64_t best_cost = 0;
   for (int64_t c = cmin; c <= cmax; c++) {
@@ -271,13 +276,14 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
                             const void* x, const void* gate, const void* up, const float* gamma, float eps,
                             const Outputs& out, void* ws, unsigned flags, void* stream, int64_t fault_unit) {
   const Geo g = make_geo(fmt, 0, K, G);  // the K geometry every weight shares
+  const int mode = p.moe ? 1 : p.codebook ? 2 : 0;
   Plan pl;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     DevCache* dc = nullptr;
     qlin_status st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, NB, bblock_bytes(g.KB, G, M), *dc, kind, p.moe != 0, &pl);
+    st = make_plan(g, NB, bblock_bytes(g.KB, G, M), *dc, kind, mode, &pl);
     if (st != QLIN_OK) return st;
   }
   p.x = static_cast<const __nv_bfloat16*>(x);
@@ -304,7 +310,7 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
   p.fault_unit = fault_unit;
   p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
   void* args[] = {&p};
-  return launch(forward_fn(g.bits, kind, G, p.moe != 0), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
+  return launch(forward_fn(g.bits, kind, G, mode), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
                 dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args, pl.C,
                 (flags & QLIN_FLAG_PDL) != 0);
 }
@@ -315,7 +321,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
                          const void* const* packed, const void* x, const void* gate, const void* up,
                          const float* gamma, float eps, float* const* ys, const float* const* biases,
                          const Outputs& out, void* ws, size_t ws_bytes, unsigned flags, void* stream, bool debug,
-                         int64_t fault_unit = -1) {
+                         int64_t fault_unit = -1, const float* codebook = nullptr) {
   if (n < 1 || n > MAX_LIN || !Ns || !packed || !ys) return QLIN_ERR_INVALID_ARG;
   qlin_status st = QLIN_OK;
   int64_t NB = 0;
@@ -352,6 +358,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
     nl++;
   }
   p.n_lin = nl;
+  p.codebook = codebook;
   return plan_and_launch(p, fmt, kind, M, K, G, NB, x, gate, up, gamma, eps, out, ws, flags, stream, fault_unit);
 }
 
@@ -552,6 +559,19 @@ qlin_status qlin_forward_moe(int fmt, int prologue, int M, int E, int64_t N, int
                   stream);
 }
 
+qlin_status qlin_forward_codebook(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G, const void* packed,
+                                  const float* codebook, const void* x, const void* gate, const void* up,
+                                  const float* gamma, float eps, const float* bias, float* y, void* ws,
+                                  size_t ws_bytes, unsigned flags, void* stream) {
+  if (fmt != QLIN_W4A8) return QLIN_ERR_INVALID_ARG;  // the format has codebooks for 4-bit codes only
+  qlin_status st = check_shape_impl(fmt, N, K, G);
+  if (st != QLIN_OK) return st;
+  if (G < 32) return QLIN_ERR_UNSUPPORTED;
+  if (!codebook || !aligned(codebook, 4)) return QLIN_ERR_INVALID_ARG;
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, &bias, Outputs(), ws,
+                      ws_bytes, flags, stream, false, -1, codebook);
+}
+
 qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, int64_t* ctas, int64_t* units,
                                      int64_t* stream_bytes) {
   qlin_status st = check_shape_impl(fmt, N, K, G);
@@ -564,7 +584,7 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, i
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, row_blocks(N), bblock_bytes(g.KB, G, MAX_M), *dc, QLIN_PROLOGUE_NONE, false, &pl);
+    st = make_plan(g, row_blocks(N), bblock_bytes(g.KB, G, MAX_M), *dc, QLIN_PROLOGUE_NONE, 0, &pl);
     if (st != QLIN_OK) return st;
   }
   *ctas = (int64_t)pl.C * pl.NB;

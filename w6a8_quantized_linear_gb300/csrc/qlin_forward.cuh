@@ -67,6 +67,7 @@ struct FwdParams {
   const uint8_t* bank;        // repacked [E * ne, K] stream
   const float* bank_bias;     // [E, ne] or null
   float* ymoe;                // [M, topk, ne]
+  const float* codebook;      // codebook mode: fp32 [16] levels of the 4-bit codes
   const __nv_bfloat16* x;     // NONE, RMSNORM: [M, K]
   const __nv_bfloat16* gate;  // SWIGLU: [M, K]
   const __nv_bfloat16* up;    // SWIGLU: [M, K]
@@ -201,11 +202,20 @@ __device__ __forceinline__ void unpack_step(uint32_t w, uint32_t h01, uint32_t h
   }
 }
 
+// Codebook levels (4-bit codes): register i's two codes (bits 4i..4i+3 and
+// 16+4i..16+4i+3) index a 256-entry table of fp16 pairs.
+__device__ __forceinline__ void unpack_step_lut(uint32_t w, const uint32_t* lut, uint32_t (&a)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; i++) a[i] = lut[((w >> (4 * i)) & 0xFu) | ((w >> (12 + 4 * i)) & 0xF0u)];
+}
+
 // One 32-wide k pair of one 16-row slab: step A into chain ca, step B into cb.
-// The first pair of a sub-group starts each chain at its start value.
-template <int BITS>
+// The first pair of a sub-group starts each chain at its start value.  With
+// a codebook (lut != null, 4-bit codes) the A registers come from the table.
+template <int BITS, bool CB = false>
 __device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uint4& bq, bool first, const float4& sA,
-                                          const float4& sB, uint32_t base, float (&ca)[4], float (&cb)[4]) {
+                                          const float4& sB, uint32_t base, float (&ca)[4], float (&cb)[4],
+                                          const uint32_t* lut = nullptr) {
   const uint2 w = *reinterpret_cast<const uint2*>(cp + lane * 8);
   uint32_t hA01 = 0, hA23 = 0, hB01 = 0, hB23 = 0;
   if (BITS == 6) {
@@ -216,8 +226,13 @@ __device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uin
     hB23 = h >> 6;
   }
   uint32_t a[4], b[4];
-  unpack_step<BITS>(w.x, hA01, hA23, base, a);
-  unpack_step<BITS>(w.y, hB01, hB23, base, b);
+  if constexpr (CB) {
+    unpack_step_lut(w.x, lut, a);
+    unpack_step_lut(w.y, lut, b);
+  } else {
+    unpack_step<BITS>(w.x, hA01, hA23, base, a);
+    unpack_step<BITS>(w.y, hB01, hB23, base, b);
+  }
   if (first) {
     mma_f16_16816_c(ca, a[0], a[1], a[2], a[3], bq.x, bq.y, sA.x, sA.y, sA.z, sA.w);
     mma_f16_16816_c(cb, b[0], b[1], b[2], b[3], bq.z, bq.w, sB.x, sB.y, sB.z, sB.w);
@@ -267,8 +282,11 @@ __device__ __forceinline__ void group_mma(const uint32_t (&a)[4], const uint32_t
   }
 }
 
-template <int BITS, int KIND, int G, bool MOE>
+// MODE: 0 plain (weight table), 1 expert bank, 2 4-bit codebook levels.
+template <int BITS, int KIND, int G, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
+  constexpr bool MOE = MODE == 1, CB = MODE == 2;
+  static_assert(!CB || (BITS == 4 && G >= PAIR_K), "codebooks: 4-bit codes, groups of 32 and more");
   // G < 32: groups are narrower than a 32-wide pair; each group is its own
   // chain (one MMA) with its own start value, GPP groups per pair.
   constexpr bool PER_STEP = G < PAIR_K;
@@ -290,6 +308,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   __shared__ __align__(16) float s_slot[MAX_CLUSTER][MAX_M][2];  // rank r's (amax, sum x^2) per row
   __shared__ float s_row[MAX_M][2];                               // s, code factor c
   __shared__ uint32_t s_tokmask[MAX_M];                            // expert bank: slots of each token
+  __shared__ uint32_t s_lut[CB ? 256 : 1];                         // codebook: fp16 pairs by code pair
+  __shared__ float s_cbscale;                                      // codebook: 2^-sh (table scaled by 2^sh)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // TMA destinations and vector loads need 16-byte alignment of the dynamic
@@ -393,6 +413,24 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   // split-K positions (consumer thread slots) this CTA owns and finishes
   const int pos0 = (int)(crank * CONSUMERS / C), pos1 = (int)((crank + 1) * CONSUMERS / C);
 
+  if constexpr (CB) {
+    // The codebook is a parameter of the weight: read before the dependency
+    // wait.  It is scaled by 2^sh so that its largest magnitude lies in
+    // [2^14, 2^15): fp16 then keeps 11 significant bits of every entry, and
+    // 2^-sh is applied (exactly) after the sums.
+    float mx = 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; c++) mx = fmaxf(mx, fabsf(__ldg(p.codebook + c)));
+    int e = 0;
+    (void)frexpf(mx, &e);
+    const int sh = mx > 0.f ? 15 - e : 0;
+    if (tid < 256) {
+      const __half2 h2 = __floats2half2_rn(ldexpf(__ldg(p.codebook + (tid & 15)), sh),
+                                           ldexpf(__ldg(p.codebook + (tid >> 4)), sh));
+      s_lut[tid] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    if (tid == 0) s_cbscale = ldexpf(1.0f, -sh);
+  }
   if (tid == 0) {
     for (int s = 0; s < S; s++) {
       mbar_init(&full_bar[s], 1);
@@ -537,7 +575,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   //      unit contributes exactly nothing from the k it does not have.
   {
     const float off = (float)code_offset(BITS);
-    const float fg = -(1024.0f + off), fg8 = -(1024.0f + 16.0f * off);  // rows g and g + 8
+    // rows g and g + 8 (no offset to remove when the levels come from a codebook)
+    const float fg = CB ? 0.f : -(1024.0f + off), fg8 = CB ? 0.f : -(1024.0f + 16.0f * off);
     const int64_t n8f = (int64_t)nu * (KB / 8);
     const int rounds2 = (int)((n8f + CONSUMERS - 1) / CONSUMERS);
     for (int r = 0; r < rounds2; r++) {
@@ -724,8 +763,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         for (int pp = 0; pp < PPS; pp++) {
           const int pr = sg * PPS + pp;
           const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * BPM + blane);
-          slab_pair<BITS>(c0p + pr * PB, lane, bq, pp == 0, sA, sB, base, a0, b0);
-          slab_pair<BITS>(c1p + pr * PB, lane, bq, pp == 0, sA, sB, base, a1, b1);
+          slab_pair<BITS, CB>(c0p + pr * PB, lane, bq, pp == 0, sA, sB, base, a0, b0, s_lut);
+          slab_pair<BITS, CB>(c1p + pr * PB, lane, bq, pp == 0, sA, sB, base, a1, b1, s_lut);
         }
 #pragma unroll
         for (int e = 0; e < 4; e++) {  // exact: integer sums below 2^24
@@ -771,10 +810,17 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       unit = tile_base;
     }
   }
+  {
+    // rows g + 8 carry a factor 16 on the positional route; a codebook's
+    // table carries 2^sh on both rows (exact powers of two)
+    const float f_lo = CB ? s_cbscale : 1.0f, f_hi = CB ? s_cbscale : 0.0625f;
 #pragma unroll
-  for (int a = 0; a < 2; a++) {  // rows g + 8 carry a factor 16 (exact power of two)
-    yacc[a][2] *= 0.0625f;
-    yacc[a][3] *= 0.0625f;
+    for (int a = 0; a < 2; a++) {
+      yacc[a][0] *= f_lo;
+      yacc[a][1] *= f_lo;
+      yacc[a][2] *= f_hi;
+      yacc[a][3] *= f_hi;
+    }
   }
 
   // ---- phase 4: split-K reduction.  Partial sums of position (warp, lane) go

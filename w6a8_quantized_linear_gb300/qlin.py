@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
                                             vp, vp, vp, sz, ctypes.c_uint, vp]),
                 "qlin_forward_moe": (st, [i32, i32, i32, i32, i64, i64, i64, vp, vp, i32, vp, vp, vp, vp,
                                           ctypes.c_float, vp, vp, vp, sz, ctypes.c_uint, vp]),
+                "qlin_forward_codebook": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                               vp, vp, vp, sz, ctypes.c_uint, vp]),
                 "qlin_forward_launch_info": (st, [i32, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                                   ctypes.POINTER(i64)]),
                 "qlin_read_device_status": (st, [vp, vp]),
@@ -221,6 +223,26 @@ def forward_moe(fmt, prologue, bank: torch.Tensor, E: int, N: int, K: int, G: in
     _check(lib().qlin_forward_moe(_fmt(fmt), _pro(prologue), M, E, N, K, G, _ptr(bank), _ptr(ids), topk, _ptr(x),
                                   _ptr(gate), _ptr(up), _ptr(gamma), float(eps), _ptr(bias), _ptr(y), _ptr(ws),
                                   ws.numel(), flags, _stream(stream)), "forward_moe")
+    return y
+
+
+def forward_codebook(fmt, prologue, packed: torch.Tensor, codebook: torch.Tensor, N: int, K: int, G: int, x=None,
+                     gate=None, up=None, gamma=None, eps: float = 1e-6, bias: torch.Tensor | None = None,
+                     y: torch.Tensor | None = None, ws: torch.Tensor | None = None, flags: int = 0,
+                     stream=None) -> torch.Tensor:
+    """``forward`` with the levels of the 4-bit codes read from ``codebook``
+    (fp32 [16] on the device) instead of code - 8; optional fp32 [N] bias."""
+    if codebook.dtype != torch.float32 or codebook.numel() != 16 or not codebook.is_contiguous():
+        raise ValueError("codebook must be a contiguous float32 tensor of 16 levels")
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.float32, device=packed.device)
+    if ws is None:
+        ws = new_workspace(forward_workspace_bytes(fmt, N, K, G), packed.device, stream)
+    _check(lib().qlin_forward_codebook(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(codebook), _ptr(x),
+                                       _ptr(gate), _ptr(up), _ptr(gamma), float(eps), _ptr(bias), _ptr(y), _ptr(ws),
+                                       ws.numel(), flags, _stream(stream)), "forward_codebook")
     return y
 
 
