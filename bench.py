@@ -440,12 +440,19 @@ def run_linear(args):
         if kind == "rmsnorm":
             gamma = torch.empty(K, device=dev).uniform_(0.5, 1.5, generator=g)
         calls.append((ws_, x, gate, up, gamma, [torch.empty(args.M, N, device=dev) for N in Ns]))
+    cb = torch.sort(torch.randn(16, generator=g, device=dev)).values if args.codebook else None
     for ws_, x, gate, up, gamma, ys in calls:
+        if cb is not None:
+            for w, N, y in zip(ws_, Ns, ys):
+                qlin.forward_codebook("w4a8", kind, w, cb, N, K, G, x=x, gate=gate, up=up, gamma=gamma, y=y, ws=ws,
+                                      flags=qlin.FLAG_PDL)
+            continue
         qlin.forward_multi("w4a8", kind, ws_, Ns, K, G, x=x, gate=gate, up=up, gamma=gamma, y=ys, ws=ws,
                            flags=qlin.FLAG_PDL)
     torch.cuda.synchronize()
     assert qlin.read_device_status(ws) == qlin.OK
     print(json.dumps({"linear": args.linear, "M": args.M, "N": Ns, "K": K, "calls": args.calls,
+                      "codebook": args.codebook,
                       "bytes_per_launch": sum(qlin.packed_bytes("w4a8", N, K, G) for N in Ns)}))
     return 0
 
@@ -462,6 +469,7 @@ def main():
     ap.add_argument("--linear", default=None, help="profile mode: one linear type of the stack")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--codebook", action="store_true", help="profile mode: levels from a 16-entry codebook")
     ap.add_argument("--print-kernel-hash", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":

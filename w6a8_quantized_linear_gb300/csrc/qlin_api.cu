@@ -129,20 +129,21 @@ struct Plan {
   int64_t stage_bytes = 0, b_off = 0, red_off = 0, smem = 0;
 };
 
-// Shared-memory carve: [stages][activation operand][split-K slots].  Fails
+// Shared-memory carve: [extra][stages][activation operand][split-K slots]
+// (extra: the codebook table, which the kernel expects at offset 0).  Fails
 // when the budget holds fewer than min_stages stages (or the CTA's units).
-bool carve(const Geo& g, int64_t bbf, Plan& pl, int64_t budget, int64_t min_stages) {
+bool carve(const Geo& g, int64_t bbf, Plan& pl, int64_t budget, int64_t min_stages, int64_t extra) {
   pl.stage_bytes = round_up(2 * g.unit_full, 128);
   const int64_t b_bytes = round_up(pl.upc * bbf, 128);
   const int64_t cmax = (CONSUMERS + pl.C - 1) / pl.C;
   const int64_t red_bytes = round_up((int64_t)pl.C * cmax * 8 * 4, 128);
-  const int64_t rest = b_bytes + red_bytes + 128;
+  const int64_t rest = b_bytes + red_bytes + extra + 128;
   int64_t st = (budget - rest) / pl.stage_bytes;
   if (st > MAX_STAGES) st = MAX_STAGES;
   if (st > pl.upc) st = pl.upc;
   if (st < (min_stages < pl.upc ? min_stages : pl.upc)) return false;
   pl.stages = (int)st;
-  pl.b_off = pl.stages * pl.stage_bytes;
+  pl.b_off = extra + pl.stages * pl.stage_bytes;
   pl.red_off = pl.b_off + b_bytes;
   pl.smem = pl.red_off + red_bytes + 128;
   return true;
@@ -192,7 +193,8 @@ qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int k
     pl.NB = NB;
     pl.C = (int)c;
     pl.upc = (int)((g.J + c - 1) / c);
-    if (!(carve(g, bbf, pl, SMEM_TWO_PER_SM, 3) || carve(g, bbf, pl, SMEM_MAX, 2))) continue;
+    const int64_t extra = mode == 2 ? CODEBOOK_LUT_BYTES : 0;
+    if (!(carve(g, bbf, pl, SMEM_TWO_PER_SM, 3, extra) || carve(g, bbf, pl, SMEM_MAX, 2, extra))) continue;
     const int n = active_clusters(dc, fn, pl.C, pl.smem);
     if (n < 1) continue;
     const int64_t cost = (NB + n - 1) / n * pl.upc;

@@ -82,7 +82,7 @@ struct FwdParams {
   float inv_k;                // 1 / K (RMSNorm mean)
   int64_t tile_full, unit_full, stage_bytes;
   int bpm, bbf;               // activation operand: bytes per 32-wide pair, per unit block
-  int64_t b_off, red_off;     // dynamic shared memory carve (bytes)
+  int64_t b_off, red_off;     // dynamic shared memory carve (bytes); stages start at stage0<MODE>()
   int stages;
   int64_t fault_unit;         // test only: unit of CTA (0,0) whose copy is never issued (-1: none)
   // fp16 1024.0 in both halves (0x64006400).  Passed as a parameter, not a
@@ -202,11 +202,29 @@ __device__ __forceinline__ void unpack_step(uint32_t w, uint32_t h01, uint32_t h
   }
 }
 
-// Codebook levels (4-bit codes): register i's two codes (bits 4i..4i+3 and
-// 16+4i..16+4i+3) index a 256-entry table of fp16 pairs.
-__device__ __forceinline__ void unpack_step_lut(uint32_t w, const uint32_t* lut, uint32_t (&a)[4]) {
-#pragma unroll
-  for (int i = 0; i < 4; i++) a[i] = lut[((w >> (4 * i)) & 0xFu) | ((w >> (12 + 4 * i)) & 0xF0u)];
+// Codebook levels (4-bit codes).  The table holds, for every byte value e
+// (codes lo = e & 15 and hi = e >> 4), the fp16 pair (level(lo), level(hi)),
+// one copy per lane: entry e of lane l at byte 128 e + 4 l, so the 32 lookups
+// of a warp fall in 32 different banks.  Byte J of a plane word holds the
+// codes of registers 2J % 4.. at one k (nibbles 2J, 2J + 1); two byte lookups
+// and a byte permute give a register's two k.
+template <int J>
+__device__ __forceinline__ uint32_t lut_byte_off(uint32_t w, uint32_t lane4) {
+  constexpr int s = 8 * J - 7;  // bits 8J..8J+7 to 7..14
+  const uint32_t v = s >= 0 ? (w >> s) : (w << -s);
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "n"(0x7F80), "r"(lane4));  // (v & mask) | lane4
+  return r;
+}
+__device__ __forceinline__ void unpack_step_lut(uint32_t w, const uint8_t* lut, uint32_t lane4, uint32_t (&a)[4]) {
+  const uint32_t x0 = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<0>(w, lane4));  // nibbles 0, 1
+  const uint32_t x1 = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<1>(w, lane4));  // 2, 3
+  const uint32_t x2 = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<2>(w, lane4));  // 4, 5
+  const uint32_t x3 = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<3>(w, lane4));  // 6, 7
+  a[0] = __byte_perm(x0, x2, 0x5410);  // register i: nibbles i and 4 + i
+  a[1] = __byte_perm(x0, x2, 0x7632);
+  a[2] = __byte_perm(x1, x3, 0x5410);
+  a[3] = __byte_perm(x1, x3, 0x7632);
 }
 
 // One 32-wide k pair of one 16-row slab: step A into chain ca, step B into cb.
@@ -215,7 +233,7 @@ __device__ __forceinline__ void unpack_step_lut(uint32_t w, const uint32_t* lut,
 template <int BITS, bool CB = false>
 __device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uint4& bq, bool first, const float4& sA,
                                           const float4& sB, uint32_t base, float (&ca)[4], float (&cb)[4],
-                                          const uint32_t* lut = nullptr) {
+                                          const uint8_t* lut = nullptr) {
   const uint2 w = *reinterpret_cast<const uint2*>(cp + lane * 8);
   uint32_t hA01 = 0, hA23 = 0, hB01 = 0, hB23 = 0;
   if (BITS == 6) {
@@ -227,8 +245,8 @@ __device__ __forceinline__ void slab_pair(const uint8_t* cp, int lane, const uin
   }
   uint32_t a[4], b[4];
   if constexpr (CB) {
-    unpack_step_lut(w.x, lut, a);
-    unpack_step_lut(w.y, lut, b);
+    unpack_step_lut(w.x, lut, (uint32_t)lane * 4, a);
+    unpack_step_lut(w.y, lut, (uint32_t)lane * 4, b);
   } else {
     unpack_step<BITS>(w.x, hA01, hA23, base, a);
     unpack_step<BITS>(w.y, hB01, hB23, base, b);
@@ -286,6 +304,10 @@ __device__ __forceinline__ void group_mma(const uint32_t (&a)[4], const uint32_t
 template <int BITS, int KIND, int G, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
   constexpr bool MOE = MODE == 1, CB = MODE == 2;
+  // dynamic shared memory: [codebook table (codebook mode)][stages][activation
+  // operand][split-K slots]; the table sits first so that its address is a
+  // constant of the kernel
+  constexpr int STAGE0 = CB ? CODEBOOK_LUT_BYTES : 0;
   static_assert(!CB || (BITS == 4 && G >= PAIR_K), "codebooks: 4-bit codes, groups of 32 and more");
   // G < 32: groups are narrower than a 32-wide pair; each group is its own
   // chain (one MMA) with its own start value, GPP groups per pair.
@@ -308,7 +330,6 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   __shared__ __align__(16) float s_slot[MAX_CLUSTER][MAX_M][2];  // rank r's (amax, sum x^2) per row
   __shared__ float s_row[MAX_M][2];                               // s, code factor c
   __shared__ uint32_t s_tokmask[MAX_M];                            // expert bank: slots of each token
-  __shared__ uint32_t s_lut[CB ? 256 : 1];                         // codebook: fp16 pairs by code pair
   __shared__ float s_cbscale;                                      // codebook: 2^-sh (table scaled by 2^sh)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -418,18 +439,23 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     // wait.  It is scaled by 2^sh so that its largest magnitude lies in
     // [2^14, 2^15): fp16 then keeps 11 significant bits of every entry, and
     // 2^-sh is applied (exactly) after the sums.
-    float mx = 0.f;
+    __shared__ uint16_t s_cb16[16];
+    if (tid < 16) {
+      float mx = 0.f;
 #pragma unroll
-    for (int c = 0; c < 16; c++) mx = fmaxf(mx, fabsf(__ldg(p.codebook + c)));
-    int e = 0;
-    (void)frexpf(mx, &e);
-    const int sh = mx > 0.f ? 15 - e : 0;
-    if (tid < 256) {
-      const __half2 h2 = __floats2half2_rn(ldexpf(__ldg(p.codebook + (tid & 15)), sh),
-                                           ldexpf(__ldg(p.codebook + (tid >> 4)), sh));
-      s_lut[tid] = *reinterpret_cast<const uint32_t*>(&h2);
+      for (int c = 0; c < 16; c++) mx = fmaxf(mx, fabsf(__ldg(p.codebook + c)));
+      int e = 0;
+      (void)frexpf(mx, &e);
+      const int sh = mx > 0.f ? 15 - e : 0;
+      s_cb16[tid] = __half_as_ushort(__float2half_rn(ldexpf(__ldg(p.codebook + tid), sh)));
+      if (tid == 0) s_cbscale = ldexpf(1.0f, -sh);
     }
-    if (tid == 0) s_cbscale = ldexpf(1.0f, -sh);
+    __syncthreads();
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem);
+    for (int i = tid; i < CODEBOOK_LUT_BYTES / 4; i += GEMV_THREADS) {
+      const int e = i >> 5;  // the same entry across a warp: broadcast reads, consecutive writes
+      lut[i] = (uint32_t)s_cb16[e & 15] | ((uint32_t)s_cb16[e >> 4] << 16);
+    }
   }
   if (tid == 0) {
     for (int s = 0; s < S; s++) {
@@ -469,7 +495,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         const int64_t j = j0 + i, W = min((int64_t)KB, p.K - j * KB);
         const uint32_t wa = (uint32_t)unit_bytes(BITS, RA, W, G);
         const uint32_t wb = hasB ? (uint32_t)unit_bytes(BITS, RB, W, G) : 0u;
-        uint8_t* st = smem + (int64_t)s * p.stage_bytes;
+        uint8_t* st = smem + STAGE0 + (int64_t)s * p.stage_bytes;
         mbar_arrive_expect_tx(&full_bar[s], wa + wb);
         issued = i + 1;
         if (!(fault_cta && i == p.fault_unit)) {  // test only: this phase never completes
@@ -694,8 +720,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   const int ng_last = W_last / G;
   const int soff0 = (sl0 * 16 + 2 * g) * 4, sgrp = nslab * 64;  // scale byte offsets: slab sl0, per group
   const uint32_t base = p.f16_base;
+  const uint8_t* lut = smem;  // codebook: the per-lane level table (at a constant address)
   const int blane = (g < M ? lane : tq) * 16;  // rows M..7 read row 0's fragments (their columns are dropped)
-  const uint8_t* tile_base = smem + tsel * p.unit_full;
+  const uint8_t* tile_base = smem + STAGE0 + tsel * p.unit_full;
   const uint8_t* unit = tile_base;
   const uint8_t* bblk = bop;
   float yacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -763,8 +790,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         for (int pp = 0; pp < PPS; pp++) {
           const int pr = sg * PPS + pp;
           const uint4 bq = *reinterpret_cast<const uint4*>(bblk + pr * BPM + blane);
-          slab_pair<BITS, CB>(c0p + pr * PB, lane, bq, pp == 0, sA, sB, base, a0, b0, s_lut);
-          slab_pair<BITS, CB>(c1p + pr * PB, lane, bq, pp == 0, sA, sB, base, a1, b1, s_lut);
+          slab_pair<BITS, CB>(c0p + pr * PB, lane, bq, pp == 0, sA, sB, base, a0, b0, lut);
+          slab_pair<BITS, CB>(c1p + pr * PB, lane, bq, pp == 0, sA, sB, base, a1, b1, lut);
         }
 #pragma unroll
         for (int e = 0; e < 4; e++) {  // exact: integer sums below 2^24

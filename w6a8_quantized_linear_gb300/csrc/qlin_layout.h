@@ -34,6 +34,7 @@ constexpr int GEMV_THREADS = CONSUMERS + 32;  // + one TMA producer warp
 constexpr int MAX_STAGES = 16;
 constexpr int MAX_CLUSTER = 16;    // CTAs splitting K for one row block
 constexpr int64_t MAX_K_PER_CTA = 4096;  // activation operand held in shared memory
+constexpr int CODEBOOK_LUT_BYTES = 256 * 32 * 4;  // codebook: 256 fp16 pairs, one copy per lane
 constexpr int WS_HEADER = 256;     // forward workspace: status word (+ reserved)
 constexpr int YPART_FLOATS = CONSUMERS * 8;  // one CTA's split-K partial of its block
 constexpr int64_t MAX_K = (int64_t)MAX_CLUSTER * MAX_K_PER_CTA;
