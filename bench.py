@@ -592,7 +592,7 @@ def main():
         "widened_paths": widened,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic["bytes_per_launch"] if traffic else None,
-                     "kernel": "qlin_forward_kernel<4,1,128,0>: the gate/up multi-weight launch, M=1, "
+                     "kernel": "qlin_forward_kernel<4,128,0> (RMSNorm prologue): the gate/up multi-weight launch, M=1, "
                                f"{gu_bytes} algorithmic bytes per launch, {gu_us:.2f} us per launch (CUDA events, "
                                "64 launches in a graph)",
                      "traffic_source": traffic["source"] if traffic else "kernel changed since the last ncu capture"},

@@ -19,10 +19,8 @@
 #include "qlin_instances.h"
 #include "qlin_repack.cuh"
 
-// the forward kernels live in qlin_kernels_{none,rmsnorm,swiglu}.cu
-QLIN_KERNELS_OF_KIND(QLIN_DECLARE_EXTERN, 0)
-QLIN_KERNELS_OF_KIND(QLIN_DECLARE_EXTERN, 1)
-QLIN_KERNELS_OF_KIND(QLIN_DECLARE_EXTERN, 2)
+// the forward kernels live in qlin_kernels_{w4,w6_codebook,moe}.cu
+QLIN_KERNELS_ALL(QLIN_DECLARE_EXTERN)
 
 using namespace qlin;
 
@@ -49,29 +47,29 @@ qlin_status cuda_status(cudaError_t e) {
   return QLIN_ERR_CUDA;
 }
 
-template <int BITS, int KIND, int G, int MODE>
+template <int BITS, int G, int MODE>
 const void* fwd_fn() {
-  return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, KIND, G, MODE>);
+  return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, G, MODE>);
 }
 // Kernels by group size index: 32, 64, 128, 256, 16, 8, 4.  Expert banks
 // (mode 1) and codebooks (mode 2, 4-bit codes) are built for G >= 32; groups
 // of 8 and 4 exist for 4-bit codes only.
-template <int BITS, int KIND, int MODE>
+template <int BITS, int MODE>
 const void* fwd_fn_g(int gi) {
   if constexpr (MODE == 2 && BITS != 4) return nullptr;
   else {
     switch (gi) {
-      case 0: return fwd_fn<BITS, KIND, 32, MODE>();
-      case 1: return fwd_fn<BITS, KIND, 64, MODE>();
-      case 2: return fwd_fn<BITS, KIND, 128, MODE>();
-      case 3: return fwd_fn<BITS, KIND, 256, MODE>();
+      case 0: return fwd_fn<BITS, 32, MODE>();
+      case 1: return fwd_fn<BITS, 64, MODE>();
+      case 2: return fwd_fn<BITS, 128, MODE>();
+      case 3: return fwd_fn<BITS, 256, MODE>();
       default: break;
     }
     if constexpr (MODE == 0) {
-      if (gi == 4) return fwd_fn<BITS, KIND, 16, 0>();
+      if (gi == 4) return fwd_fn<BITS, 16, 0>();
       if constexpr (BITS == 4) {
-        if (gi == 5) return fwd_fn<BITS, KIND, 8, 0>();
-        return fwd_fn<BITS, KIND, 4, 0>();
+        if (gi == 5) return fwd_fn<BITS, 8, 0>();
+        return fwd_fn<BITS, 4, 0>();
       }
     }
     return nullptr;
@@ -81,15 +79,14 @@ int g_index(int64_t G) {
   return G == 32 ? 0 : G == 64 ? 1 : G == 128 ? 2 : G == 256 ? 3 : G == 16 ? 4 : G == 8 ? 5 : 6;
 }
 template <int MODE>
-const void* forward_fn_t(int bits, int kind, int64_t G) {
+const void* forward_fn_t(int bits, int64_t G) {
   const int gi = g_index(G);
-  if (bits == 6)
-    return kind == 0 ? fwd_fn_g<6, 0, MODE>(gi) : kind == 1 ? fwd_fn_g<6, 1, MODE>(gi) : fwd_fn_g<6, 2, MODE>(gi);
-  return kind == 0 ? fwd_fn_g<4, 0, MODE>(gi) : kind == 1 ? fwd_fn_g<4, 1, MODE>(gi) : fwd_fn_g<4, 2, MODE>(gi);
+  return bits == 6 ? fwd_fn_g<6, MODE>(gi) : fwd_fn_g<4, MODE>(gi);
 }
-const void* forward_fn(int bits, int kind, int64_t G, int mode = 0) {
-  return mode == 1 ? forward_fn_t<1>(bits, kind, G) : mode == 2 ? forward_fn_t<2>(bits, kind, G)
-                                                                : forward_fn_t<0>(bits, kind, G);
+// The kernel for a format, group size and mode (the prologue kind is a
+// launch parameter).
+const void* forward_fn(int bits, int64_t G, int mode = 0) {
+  return mode == 1 ? forward_fn_t<1>(bits, G) : mode == 2 ? forward_fn_t<2>(bits, G) : forward_fn_t<0>(bits, G);
 }
 
 // Per-device set-up: SM count, and the kernel attributes every launch relies on
@@ -104,16 +101,15 @@ qlin_status device_cache(DevCache** out) {
     e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_status(e);
     for (int bits : {4, 6})
-      for (int kind = 0; kind < 3; kind++)
-        for (int64_t G : {4, 8, 16, 32, 64, 128, 256})
-          for (int mode = 0; mode < 3; mode++) {
-            const void* fn = forward_fn(bits, kind, G, mode);
-            if (!fn) continue;
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
-            if (e != cudaSuccess) return cuda_status(e);
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return cuda_status(e);
-          }
+      for (int64_t G : {4, 8, 16, 32, 64, 128, 256})
+        for (int mode = 0; mode < 3; mode++) {
+          const void* fn = forward_fn(bits, G, mode);
+          if (!fn) continue;
+          e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
+          if (e != cudaSuccess) return cuda_status(e);
+          e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+          if (e != cudaSuccess) return cuda_status(e);
+        }
     c.init = true;
   }
   *out = &c;
@@ -180,12 +176,12 @@ int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
 // clusters the device holds at once give the waves of the launch; the cost is
 // waves x stream units of the busiest CTA.  The cheapest C wins, ties going
 // to the smaller cluster.  Caller holds g_mu.
-qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int kind, int mode, Plan* out) {
+qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int mode, Plan* out) {
   const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
   const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
   const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
   if (cmin > cmax) return QLIN_ERR_UNSUPPORTED;
-  const void* fn = forward_fn(g.bits, kind, g.G, mode);
+  const void* fn = forward_fn(g.bits, g.G, mode);
   bool found = false;
   int64_t best_cost = 0;
   for (int64_t c = cmin; c <= cmax; c++) {
@@ -285,7 +281,7 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
     DevCache* dc = nullptr;
     qlin_status st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, NB, bblock_bytes(g.KB, G, M), *dc, kind, mode, &pl);
+    st = make_plan(g, NB, bblock_bytes(g.KB, G, M), *dc, mode, &pl);
     if (st != QLIN_OK) return st;
   }
   p.x = static_cast<const __nv_bfloat16*>(x);
@@ -298,6 +294,7 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
   p.q_out = out.q;
   p.s_out = out.s;
   p.M = M;
+  p.kind = kind;
   p.K = K;
   p.inv_k = 1.0f / (float)K;
   p.J = g.J;
@@ -312,7 +309,7 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
   p.fault_unit = fault_unit;
   p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
   void* args[] = {&p};
-  return launch(forward_fn(g.bits, kind, G, mode), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
+  return launch(forward_fn(g.bits, G, mode), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
                 dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args, pl.C,
                 (flags & QLIN_FLAG_PDL) != 0);
 }
@@ -586,7 +583,7 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, i
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, row_blocks(N), bblock_bytes(g.KB, G, MAX_M), *dc, QLIN_PROLOGUE_NONE, 0, &pl);
+    st = make_plan(g, row_blocks(N), bblock_bytes(g.KB, G, MAX_M), *dc, 0, &pl);
     if (st != QLIN_OK) return st;
   }
   *ctas = (int64_t)pl.C * pl.NB;

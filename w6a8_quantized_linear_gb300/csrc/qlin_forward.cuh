@@ -78,11 +78,12 @@ struct FwdParams {
   int8_t* q_out;              // test export: [M, K] activation codes
   float* s_out;               // test export: [M] row scales
   int M;
+  int kind;                   // prologue: 0 none, 1 RMSNorm, 2 SwiGLU
   int64_t K, J;
   float inv_k;                // 1 / K (RMSNorm mean)
   int64_t tile_full, unit_full, stage_bytes;
   int bpm, bbf;               // activation operand: bytes per 32-wide pair, per unit block
-  int64_t b_off, red_off;     // dynamic shared memory carve (bytes); stages start at stage0<MODE>()
+  int64_t b_off, red_off;     // dynamic shared memory carve (bytes; the codebook table, if any, precedes the stages)
   int stages;
   int64_t fault_unit;         // test only: unit of CTA (0,0) whose copy is never issued (-1: none)
   // fp16 1024.0 in both halves (0x64006400).  Passed as a parameter, not a
@@ -116,6 +117,12 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 r, float (&v)[8]) {
 // the model like the weights, is loaded separately (possibly before that
 // kernel completes, under QLIN_FLAG_PDL).  SwiGLU values are computed once, at
 // load, and kept in fp32.
+template <int K>
+struct KindTag {
+  static constexpr int value = K;
+};
+
+// One thread's 8-wide K slice of every row, for prologue kind KIND.
 template <int KIND>
 struct ActSlice {
   uint4 a[KIND == 2 ? 1 : MAX_M];     // x (NONE, RMSNORM)
@@ -301,7 +308,7 @@ __device__ __forceinline__ void group_mma(const uint32_t (&a)[4], const uint32_t
 }
 
 // MODE: 0 plain (weight table), 1 expert bank, 2 4-bit codebook levels.
-template <int BITS, int KIND, int G, int MODE>
+template <int BITS, int G, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
   constexpr bool MOE = MODE == 1, CB = MODE == 2;
   // dynamic shared memory: [codebook table (codebook mode)][stages][activation
@@ -520,183 +527,196 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   // -------------------------------------------------------------------- consumers
   uint8_t* bop = smem + p.b_off;  // activation operand blocks, one per unit of this CTA
   const int rounds = (int)((n8 + CONSUMERS - 1) / CONSUMERS);
-  ActSlice<KIND> act;
-  if (tid < n8) act.load_gamma(p, k_lo + tid * 8);  // a model parameter: may be read early
-  pdl_wait();  // activations may be written by the previous kernel in the stream
+  // Phases 1 and 2 are specialised per prologue kind: the kind is a launch
+  // parameter (uniform across the grid), so one kernel serves every kind and
+  // consecutive launches of different prologues run the same main loop code.
+  auto prologue = [&](auto kind_tag) {
+    constexpr int KIND = decltype(kind_tag)::value;
+    ActSlice<KIND> act;
+    if (tid < n8) act.load_gamma(p, k_lo + tid * 8);  // a model parameter: may be read early
+    pdl_wait();  // activations may be written by the previous kernel in the stream
 
-  // ---- phase 1: prologue statistics of this CTA's K range, per row
-  {
-    float amax[MAX_M], ssq[MAX_M];
-#pragma unroll
-    for (int m = 0; m < MAX_M; m++) amax[m] = ssq[m] = 0.f;
-    for (int r = 0; r < rounds; r++) {
-      const int64_t i8 = (int64_t)r * CONSUMERS + tid;
-      if (i8 < n8) {
-        if (r > 0) act.load_gamma(p, k_lo + i8 * 8);
-        act.load(p, M, k_lo + i8 * 8);
-#pragma unroll
-        for (int m = 0; m < MAX_M; m++) {
-          if (m < M) {
-            float v[8];
-            act.value(m, v, ssq[m]);
-#pragma unroll
-            for (int e = 0; e < 8; e++) amax[m] = fmaxf(amax[m], fabsf(v[e]));
+    // ---- phase 1: prologue statistics of this CTA's K range, per row
+    {
+      float amax[MAX_M], ssq[MAX_M];
+  #pragma unroll
+      for (int m = 0; m < MAX_M; m++) amax[m] = ssq[m] = 0.f;
+      for (int r = 0; r < rounds; r++) {
+        const int64_t i8 = (int64_t)r * CONSUMERS + tid;
+        if (i8 < n8) {
+          if (r > 0) act.load_gamma(p, k_lo + i8 * 8);
+          act.load(p, M, k_lo + i8 * 8);
+  #pragma unroll
+          for (int m = 0; m < MAX_M; m++) {
+            if (m < M) {
+              float v[8];
+              act.value(m, v, ssq[m]);
+  #pragma unroll
+              for (int e = 0; e < 8; e++) amax[m] = fmaxf(amax[m], fabsf(v[e]));
+            }
           }
         }
       }
-    }
-#pragma unroll
-    for (int m = 0; m < MAX_M; m++) {
-      if (m < M) {
-        const float a = warp_max(amax[m]);
-        const float q = KIND == 1 ? warp_sum(ssq[m]) : 0.f;
-        if (lane == 0) {
-          s_red[warp][m][0] = a;
-          s_red[warp][m][1] = q;
-        }
-      }
-    }
-  }
-  consumer_bar();
-  cluster_wait();  // every CTA of the cluster has initialised its barriers
-  if (tid < M) {
-    float a = 0.f, q = 0.f;
-    for (int w = 0; w < CONSUMER_WARPS; w++) {  // fixed order
-      a = fmaxf(a, s_red[w][tid][0]);
-      q = __fadd_rn(q, s_red[w][tid][1]);
-    }
-    const uint32_t local = smem_u32(&s_slot[crank][tid][0]), lbar = smem_u32(&stat_bar);
-    for (int r = 0; r < C; r++) st_async_f2(dsmem_addr_u32(local, r), a, q, dsmem_addr_u32(lbar, r));
-  }
-  if (!mbar_wait_cluster(&stat_bar, 0) && lane == 0) atomicExch(p.status, 4u);
-  if (tid < M) {
-    float a = 0.f, q = 0.f;
-    for (int r = 0; r < C; r++) {  // fixed rank order: the same sums in every CTA
-      a = fmaxf(a, s_slot[r][tid][0]);
-      q = __fadd_rn(q, s_slot[r][tid][1]);
-    }
-    // Row scale s and the factor c that maps a prologue value to its code
-    // (a * c = a / s).  With no prologue s and the quotients are IEEE, so the
-    // codes equal the definition bit for bit; with a prologue the tolerance
-    // of the method allows the fast reciprocal forms.
-    float s, c;
-    if (KIND == 0) {
-      s = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
-      c = 0.f;
-    } else {
-      const float rs = KIND == 1 ? rsqrtf(__fadd_rn(__fmul_rn(q, p.inv_k), p.eps)) : 1.0f;
-      const float amax = __fmul_rn(a, rs);  // = max |fl(x*gamma) * rstd| (rounding is monotone)
-      s = amax * (1.0f / 127.0f);
-      c = amax > 0.f ? __fmul_rn(rs, __fdividef(127.0f, amax)) : 0.f;
-    }
-    s_row[tid][0] = s;
-    s_row[tid][1] = c;
-    if (p.s_out && blockIdx.y == 0 && crank == 0) p.s_out[tid] = s;
-  }
-  consumer_bar();
-
-  // ---- phase 2: quantise this CTA's K range into the MMA B operand (fp16),
-  //      plus each sub-group's chain start values.  Every block is written
-  //      over its full width: past K the codes are zero, so a narrower last
-  //      unit contributes exactly nothing from the k it does not have.
-  {
-    const float off = (float)code_offset(BITS);
-    // rows g and g + 8 (no offset to remove when the levels come from a codebook)
-    const float fg = CB ? 0.f : -(1024.0f + off), fg8 = CB ? 0.f : -(1024.0f + 16.0f * off);
-    const int64_t n8f = (int64_t)nu * (KB / 8);
-    const int rounds2 = (int)((n8f + CONSUMERS - 1) / CONSUMERS);
-    for (int r = 0; r < rounds2; r++) {
-      const int64_t i8 = (int64_t)r * CONSUMERS + tid;
-      const bool inb = i8 < n8f, valid = i8 < n8;
-      if (valid && rounds > 1) {
-        act.load_gamma(p, k_lo + i8 * 8);
-        act.load(p, M, k_lo + i8 * 8);
-      }
-      const int64_t kl = i8 * 8, jl = kl / KB;
-      const int kin = (int)(kl - jl * KB);
-      uint8_t* blk = bop + jl * p.bbf;
-      const int pr = kin / PAIR_K, step = (kin / KSTEP) & 1, half = (kin % KSTEP) >= 8;
-      float rowsum[MAX_M], rowlo[MAX_M];  // rowlo: k 0..3 of the 8 (groups of 4)
-#pragma unroll
+  #pragma unroll
       for (int m = 0; m < MAX_M; m++) {
-        rowsum[m] = 0.f;
-        rowlo[m] = 0.f;
-        if (inb && m < M) {
-          float qf[8];
-          if (valid) {
-            float v[8], ss = 0.f;
-            act.value(m, v, ss);
-            const float s = s_row[m][0], c = s_row[m][1];
-            // |t| <= 127 (1 + a few ulp) because |a| <= amax, so round half to
-            // even never leaves [-127, 127]: no clamp is needed
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-              float t;
-              if (KIND == 0) {
-                t = s > 0.f ? __fdiv_rn(v[e], s) : 0.f;  // IEEE division: codes identical to the definition
-              } else {
-                t = __fmul_rn(v[e], c);
-              }
-              const float q = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);  // round half to even
-              qf[e] = q;
-              rowsum[m] += q;
-              if (G == 4 && e < 4) rowlo[m] += q;
-            }
-            if (p.q_out && blockIdx.y == 0) {
-#pragma unroll
-              for (int e = 0; e < 8; e++) p.q_out[(int64_t)m * p.K + k_lo + kl + e] = (int8_t)(int)qf[e];
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; e++) qf[e] = 0.f;
-          }
-#pragma unroll
-          for (int t = 0; t < 4; t++) {
-            const __half2 h2 = __floats2half2_rn(qf[2 * t], qf[2 * t + 1]);  // exact: |q| <= 127
-            *reinterpret_cast<__half2*>(blk + pr * BPM + (4 * m + t) * 16 + step * 8 + half * 4) = h2;
+        if (m < M) {
+          const float a = warp_max(amax[m]);
+          const float q = KIND == 1 ? warp_sum(ssq[m]) : 0.f;
+          if (lane == 0) {
+            s_red[warp][m][0] = a;
+            s_red[warp][m][1] = q;
           }
         }
       }
-      if constexpr (G < 16) {
-        // a thread's 8 k hold one group (G = 8) or two (G = 4): no exchange
-        if (inb) {
-#pragma unroll
-          for (int hq = 0; hq < 8 / G; hq++) {
-            const int gp = (kin % PAIR_K) / G + hq;
-            float* cin = reinterpret_cast<float*>(blk + CIN + (pr * GPP + gp) * 64);
-#pragma unroll
-            for (int t = 0; t < 4; t++) {
-              float s0 = 0.f, s1 = 0.f;
-              if (2 * t < M) s0 = G == 4 ? (hq == 0 ? rowlo[2 * t] : rowsum[2 * t] - rowlo[2 * t]) : rowsum[2 * t];
-              if (2 * t + 1 < M)
-                s1 = G == 4 ? (hq == 0 ? rowlo[2 * t + 1] : rowsum[2 * t + 1] - rowlo[2 * t + 1]) : rowsum[2 * t + 1];
-              reinterpret_cast<float4*>(cin)[t] = make_float4(fg * s0, fg * s1, fg8 * s0, fg8 * s1);
-            }
-          }
-        }
+    }
+    consumer_bar();
+    cluster_wait();  // every CTA of the cluster has initialised its barriers
+    if (tid < M) {
+      float a = 0.f, q = 0.f;
+      for (int w = 0; w < CONSUMER_WARPS; w++) {  // fixed order
+        a = fmaxf(a, s_red[w][tid][0]);
+        q = __fadd_rn(q, s_red[w][tid][1]);
+      }
+      const uint32_t local = smem_u32(&s_slot[crank][tid][0]), lbar = smem_u32(&stat_bar);
+      for (int r = 0; r < C; r++) st_async_f2(dsmem_addr_u32(local, r), a, q, dsmem_addr_u32(lbar, r));
+    }
+    if (!mbar_wait_cluster(&stat_bar, 0) && lane == 0) atomicExch(p.status, 4u);
+    if (tid < M) {
+      float a = 0.f, q = 0.f;
+      for (int r = 0; r < C; r++) {  // fixed rank order: the same sums in every CTA
+        a = fmaxf(a, s_slot[r][tid][0]);
+        q = __fadd_rn(q, s_slot[r][tid][1]);
+      }
+      // Row scale s and the factor c that maps a prologue value to its code
+      // (a * c = a / s).  With no prologue s and the quotients are IEEE, so the
+      // codes equal the definition bit for bit; with a prologue the tolerance
+      // of the method allows the fast reciprocal forms.
+      float s, c;
+      if (KIND == 0) {
+        s = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+        c = 0.f;
       } else {
-      // lanes [SEG*i, SEG*(i+1)) hold one sub-group's 8-k slices; lane bit 1
-      // is the k-step, so summing over the other bits gives each chain's sum
-#pragma unroll
-      for (int m = 0; m < MAX_M; m++) {
-        if (m < M) {  // M is the same in every lane
-#pragma unroll
-          for (int o = 1; o < SEG; o <<= 1)
-            if (o != 2) rowsum[m] += __shfl_xor_sync(0xffffffffu, rowsum[m], o);
-        }
+        const float rs = KIND == 1 ? rsqrtf(__fadd_rn(__fmul_rn(q, p.inv_k), p.eps)) : 1.0f;
+        const float amax = __fmul_rn(a, rs);  // = max |fl(x*gamma) * rstd| (rounding is monotone)
+        s = amax * (1.0f / 127.0f);
+        c = amax > 0.f ? __fmul_rn(rs, __fdividef(127.0f, amax)) : 0.f;
       }
-      if (inb && (lane % SEG) < 4 && (lane & 1) == 0) {
-        const int chain = (lane >> 1) & 1;
-        float* cin = reinterpret_cast<float*>(blk + CIN + (kin / SG) * 128 + chain * 64);
-#pragma unroll
-        for (int t = 0; t < 4; t++) {
-          const float s0 = 2 * t < M ? rowsum[2 * t] : 0.f;
-          const float s1 = 2 * t + 1 < M ? rowsum[2 * t + 1] : 0.f;
-          reinterpret_cast<float4*>(cin)[t] = make_float4(fg * s0, fg * s1, fg8 * s0, fg8 * s1);
+      s_row[tid][0] = s;
+      s_row[tid][1] = c;
+      if (p.s_out && blockIdx.y == 0 && crank == 0) p.s_out[tid] = s;
+    }
+    consumer_bar();
+
+    // ---- phase 2: quantise this CTA's K range into the MMA B operand (fp16),
+    //      plus each sub-group's chain start values.  Every block is written
+    //      over its full width: past K the codes are zero, so a narrower last
+    //      unit contributes exactly nothing from the k it does not have.
+    {
+      const float off = (float)code_offset(BITS);
+      // rows g and g + 8 (no offset to remove when the levels come from a codebook)
+      const float fg = CB ? 0.f : -(1024.0f + off), fg8 = CB ? 0.f : -(1024.0f + 16.0f * off);
+      const int64_t n8f = (int64_t)nu * (KB / 8);
+      const int rounds2 = (int)((n8f + CONSUMERS - 1) / CONSUMERS);
+      for (int r = 0; r < rounds2; r++) {
+        const int64_t i8 = (int64_t)r * CONSUMERS + tid;
+        const bool inb = i8 < n8f, valid = i8 < n8;
+        if (valid && rounds > 1) {
+          act.load_gamma(p, k_lo + i8 * 8);
+          act.load(p, M, k_lo + i8 * 8);
         }
-      }
+        const int64_t kl = i8 * 8, jl = kl / KB;
+        const int kin = (int)(kl - jl * KB);
+        uint8_t* blk = bop + jl * p.bbf;
+        const int pr = kin / PAIR_K, step = (kin / KSTEP) & 1, half = (kin % KSTEP) >= 8;
+        float rowsum[MAX_M], rowlo[MAX_M];  // rowlo: k 0..3 of the 8 (groups of 4)
+  #pragma unroll
+        for (int m = 0; m < MAX_M; m++) {
+          rowsum[m] = 0.f;
+          rowlo[m] = 0.f;
+          if (inb && m < M) {
+            float qf[8];
+            if (valid) {
+              float v[8], ss = 0.f;
+              act.value(m, v, ss);
+              const float s = s_row[m][0], c = s_row[m][1];
+              // |t| <= 127 (1 + a few ulp) because |a| <= amax, so round half to
+              // even never leaves [-127, 127]: no clamp is needed
+  #pragma unroll
+              for (int e = 0; e < 8; e++) {
+                float t;
+                if (KIND == 0) {
+                  t = s > 0.f ? __fdiv_rn(v[e], s) : 0.f;  // IEEE division: codes identical to the definition
+                } else {
+                  t = __fmul_rn(v[e], c);
+                }
+                const float q = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);  // round half to even
+                qf[e] = q;
+                rowsum[m] += q;
+                if (G == 4 && e < 4) rowlo[m] += q;
+              }
+              if (p.q_out && blockIdx.y == 0) {
+  #pragma unroll
+                for (int e = 0; e < 8; e++) p.q_out[(int64_t)m * p.K + k_lo + kl + e] = (int8_t)(int)qf[e];
+              }
+            } else {
+  #pragma unroll
+              for (int e = 0; e < 8; e++) qf[e] = 0.f;
+            }
+  #pragma unroll
+            for (int t = 0; t < 4; t++) {
+              const __half2 h2 = __floats2half2_rn(qf[2 * t], qf[2 * t + 1]);  // exact: |q| <= 127
+              *reinterpret_cast<__half2*>(blk + pr * BPM + (4 * m + t) * 16 + step * 8 + half * 4) = h2;
+            }
+          }
+        }
+        if constexpr (G < 16) {
+          // a thread's 8 k hold one group (G = 8) or two (G = 4): no exchange
+          if (inb) {
+  #pragma unroll
+            for (int hq = 0; hq < 8 / G; hq++) {
+              const int gp = (kin % PAIR_K) / G + hq;
+              float* cin = reinterpret_cast<float*>(blk + CIN + (pr * GPP + gp) * 64);
+  #pragma unroll
+              for (int t = 0; t < 4; t++) {
+                float s0 = 0.f, s1 = 0.f;
+                if (2 * t < M) s0 = G == 4 ? (hq == 0 ? rowlo[2 * t] : rowsum[2 * t] - rowlo[2 * t]) : rowsum[2 * t];
+                if (2 * t + 1 < M)
+                  s1 = G == 4 ? (hq == 0 ? rowlo[2 * t + 1] : rowsum[2 * t + 1] - rowlo[2 * t + 1]) : rowsum[2 * t + 1];
+                reinterpret_cast<float4*>(cin)[t] = make_float4(fg * s0, fg * s1, fg8 * s0, fg8 * s1);
+              }
+            }
+          }
+        } else {
+        // lanes [SEG*i, SEG*(i+1)) hold one sub-group's 8-k slices; lane bit 1
+        // is the k-step, so summing over the other bits gives each chain's sum
+  #pragma unroll
+        for (int m = 0; m < MAX_M; m++) {
+          if (m < M) {  // M is the same in every lane
+  #pragma unroll
+            for (int o = 1; o < SEG; o <<= 1)
+              if (o != 2) rowsum[m] += __shfl_xor_sync(0xffffffffu, rowsum[m], o);
+          }
+        }
+        if (inb && (lane % SEG) < 4 && (lane & 1) == 0) {
+          const int chain = (lane >> 1) & 1;
+          float* cin = reinterpret_cast<float*>(blk + CIN + (kin / SG) * 128 + chain * 64);
+  #pragma unroll
+          for (int t = 0; t < 4; t++) {
+            const float s0 = 2 * t < M ? rowsum[2 * t] : 0.f;
+            const float s1 = 2 * t + 1 < M ? rowsum[2 * t + 1] : 0.f;
+            reinterpret_cast<float4*>(cin)[t] = make_float4(fg * s0, fg * s1, fg8 * s0, fg8 * s1);
+          }
+        }
+        }
       }
     }
+  };
+  if (p.kind == 0) {
+    prologue(KindTag<0>{});
+  } else if (p.kind == 1) {
+    prologue(KindTag<1>{});
+  } else {
+    prologue(KindTag<2>{});
   }
   consumer_bar();
 
