@@ -19,7 +19,7 @@
 #include "qlin_instances.h"
 #include "qlin_repack.cuh"
 
-// the forward kernels live in qlin_kernels_{w4,w6_codebook,moe}.cu
+// the forward kernels live in qlin_kernels_{w4,w6_codebook,moe,export}.cu
 QLIN_KERNELS_ALL(QLIN_DECLARE_EXTERN)
 
 using namespace qlin;
@@ -52,8 +52,9 @@ const void* fwd_fn() {
   return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, G, MODE>);
 }
 // Kernels by group size index: 32, 64, 128, 256, 16, 8, 4.  Expert banks
-// (mode 1) and codebooks (mode 2, 4-bit codes) are built for G >= 32; groups
-// of 8 and 4 exist for 4-bit codes only.
+// (mode 1) and codebooks (mode 2, 4-bit codes) are built for G >= 32, the
+// plain modes (0, and 3 with the test exports) for every G; groups of 8 and
+// 4 exist for 4-bit codes only.
 template <int BITS, int MODE>
 const void* fwd_fn_g(int gi) {
   if constexpr (MODE == 2 && BITS != 4) return nullptr;
@@ -65,11 +66,11 @@ const void* fwd_fn_g(int gi) {
       case 3: return fwd_fn<BITS, 256, MODE>();
       default: break;
     }
-    if constexpr (MODE == 0) {
-      if (gi == 4) return fwd_fn<BITS, 16, 0>();
+    if constexpr (MODE == 0 || MODE == 3) {
+      if (gi == 4) return fwd_fn<BITS, 16, MODE>();
       if constexpr (BITS == 4) {
-        if (gi == 5) return fwd_fn<BITS, 8, 0>();
-        return fwd_fn<BITS, 4, 0>();
+        if (gi == 5) return fwd_fn<BITS, 8, MODE>();
+        return fwd_fn<BITS, 4, MODE>();
       }
     }
     return nullptr;
@@ -86,7 +87,10 @@ const void* forward_fn_t(int bits, int64_t G) {
 // The kernel for a format, group size and mode (the prologue kind is a
 // launch parameter).
 const void* forward_fn(int bits, int64_t G, int mode = 0) {
-  return mode == 1 ? forward_fn_t<1>(bits, G) : mode == 2 ? forward_fn_t<2>(bits, G) : forward_fn_t<0>(bits, G);
+  return mode == 1   ? forward_fn_t<1>(bits, G)
+         : mode == 2 ? forward_fn_t<2>(bits, G)
+         : mode == 3 ? forward_fn_t<3>(bits, G)
+                     : forward_fn_t<0>(bits, G);
 }
 
 // Per-device set-up: SM count, and the kernel attributes every launch relies on
@@ -102,7 +106,7 @@ qlin_status device_cache(DevCache** out) {
     if (e != cudaSuccess) return cuda_status(e);
     for (int bits : {4, 6})
       for (int64_t G : {4, 8, 16, 32, 64, 128, 256})
-        for (int mode = 0; mode < 3; mode++) {
+        for (int mode = 0; mode < 4; mode++) {
           const void* fn = forward_fn(bits, G, mode);
           if (!fn) continue;
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
@@ -274,7 +278,8 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
                             const void* x, const void* gate, const void* up, const float* gamma, float eps,
                             const Outputs& out, void* ws, unsigned flags, void* stream, int64_t fault_unit) {
   const Geo g = make_geo(fmt, 0, K, G);  // the K geometry every weight shares
-  const int mode = p.moe ? 1 : p.codebook ? 2 : 0;
+  const bool test_hooks = out.acc || out.q || out.s || fault_unit >= 0;
+  const int mode = p.moe ? 1 : p.codebook ? 2 : test_hooks ? 3 : 0;
   Plan pl;
   {
     std::lock_guard<std::mutex> lock(g_mu);

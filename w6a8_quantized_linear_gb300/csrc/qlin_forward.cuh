@@ -307,10 +307,13 @@ __device__ __forceinline__ void group_mma(const uint32_t (&a)[4], const uint32_t
   }
 }
 
-// MODE: 0 plain (weight table), 1 expert bank, 2 4-bit codebook levels.
+// MODE: 0 plain (weight table), 1 expert bank, 2 4-bit codebook levels,
+// 3 plain with the test hooks (activation codes, row scales and exact group
+// sums exported; one weight copy withheld), kept out of the other modes so
+// that their hot code stays compact.
 template <int BITS, int G, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
-  constexpr bool MOE = MODE == 1, CB = MODE == 2;
+  constexpr bool MOE = MODE == 1, CB = MODE == 2, EXPORT = MODE == 3;
   // dynamic shared memory: [codebook table (codebook mode)][stages][activation
   // operand][split-K slots]; the table sits first so that its address is a
   // constant of the kernel
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       const uint8_t* srcA = packed + tA * p.tile_full;
       const uint8_t* srcB = srcA + p.tile_full;
       const int64_t strideA = unit_bytes(BITS, RA, KB, G), strideB = unit_bytes(BITS, RB, KB, G);
-      const bool fault_cta = blockIdx.x == 0 && blockIdx.y == 0;
+      const bool fault_cta = EXPORT && blockIdx.x == 0 && blockIdx.y == 0;
       bool ok = true;
       int issued = 0, s = 0;
       uint32_t ph = 0;
@@ -603,7 +606,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       }
       s_row[tid][0] = s;
       s_row[tid][1] = c;
-      if (p.s_out && blockIdx.y == 0 && crank == 0) p.s_out[tid] = s;
+      if (EXPORT && p.s_out && blockIdx.y == 0 && crank == 0) p.s_out[tid] = s;
     }
     consumer_bar();
 
@@ -654,7 +657,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
                 rowsum[m] += q;
                 if (G == 4 && e < 4) rowlo[m] += q;
               }
-              if (p.q_out && blockIdx.y == 0) {
+              if (EXPORT && p.q_out && blockIdx.y == 0) {
   #pragma unroll
                 for (int e = 0; e < 8; e++) p.q_out[(int64_t)m * p.K + k_lo + kl + e] = (int8_t)(int)qf[e];
               }
@@ -783,7 +786,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
             yacc[a][1] = __fmaf_rn(sw.x, d[1], yacc[a][1]);
             yacc[a][2] = __fmaf_rn(sw.y, d[2], yacc[a][2]);
             yacc[a][3] = __fmaf_rn(sw.y, d[3], yacc[a][3]);
-            if (p.acc_out && gi < ng && sl0 + a < nslab) {  // test export: exact group sums
+            if (EXPORT && p.acc_out && gi < ng && sl0 + a < nslab) {  // test export: exact group sums
               const int64_t NG = p.K / G, gg = ((j0 + i) * KB) / G + gi;
               const int64_t n0 = t * TILE_N + (sl0 + a) * SLAB + g;
 #pragma unroll
@@ -830,7 +833,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       yacc[1][1] = __fmaf_rn(sw1.x, d1[1], yacc[1][1]);
       yacc[1][2] = __fmaf_rn(sw1.y, d1[2], yacc[1][2]);
       yacc[1][3] = __fmaf_rn(sw1.y, d1[3], yacc[1][3]);
-      if (p.acc_out && gi < ng) {  // test export: exact group sums
+      if (EXPORT && p.acc_out && gi < ng) {  // test export: exact group sums
         const int64_t NG = p.K / G, gg = ((j0 + i) * KB) / G + gi;
 #pragma unroll
         for (int a = 0; a < 2; a++) {
