@@ -143,7 +143,7 @@ def max_over_ranks(v: float, ws: int, device) -> float:
 # kernel reports no traffic until it is captured again.
 KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
 TRAFFIC = {
-    "bdf2ee4806d33905": {"bytes_per_launch": 97653248,
+    "f9abac9b6e2dc4ab": {"bytes_per_launch": 97588992,
                          "source": "profiles/forward_gate_up_w4a8_k5120.md (ncu --set full, one gate/up launch)"},
 }
 

@@ -1,7 +1,7 @@
 """Build libqlin.so (sm_103a) in-tree with nvcc.
 
-Five translation units compiled in parallel (the host API with the repack
-kernels, and four sets of forward-kernel variants), one
+Eight translation units compiled in parallel (the host API with the repack
+kernels, and seven sets of forward-kernel variants), one
 -gencode, shared CUDA runtime (so the library and PyTorch share one runtime
 and one notion of the current device).  The output goes to
 ``w6a8_quantized_linear_gb300/_build/libqlin.so`` (git-ignored).
@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libqlin.so")
-UNITS = ["qlin_api.cu", "qlin_kernels_w4.cu", "qlin_kernels_w6_codebook.cu", "qlin_kernels_moe.cu",
-         "qlin_kernels_export.cu"]
+UNITS = ["qlin_api.cu", "qlin_kernels_w4.cu", "qlin_kernels_w6.cu", "qlin_kernels_codebook.cu",
+         "qlin_kernels_moe_w4.cu", "qlin_kernels_moe_w6.cu", "qlin_kernels_export_w4.cu", "qlin_kernels_export_w6.cu"]
 SOURCES = [os.path.join(CSRC, f) for f in UNITS + ["qlin_forward.cuh", "qlin_repack.cuh", "qlin_layout.h",
                                                    "qlin_ptx.cuh", "qlin_instances.h"]] + [
     os.path.join(INCLUDE, "qlin.h")]

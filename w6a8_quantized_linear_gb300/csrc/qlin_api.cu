@@ -19,7 +19,7 @@
 #include "qlin_instances.h"
 #include "qlin_repack.cuh"
 
-// the forward kernels live in qlin_kernels_{w4,w6_codebook,moe,export}.cu
+// the forward kernels live in the qlin_kernels_*.cu translation units
 QLIN_KERNELS_ALL(QLIN_DECLARE_EXTERN)
 
 using namespace qlin;

@@ -122,11 +122,12 @@ struct KindTag {
   static constexpr int value = K;
 };
 
-// One thread's 8-wide K slice of every row, for prologue kind KIND.
-template <int KIND>
+// One thread's 8-wide K slice of every row, for prologue kind KIND and at
+// most MT rows.
+template <int KIND, int MT>
 struct ActSlice {
-  uint4 a[KIND == 2 ? 1 : MAX_M];     // x (NONE, RMSNORM)
-  float v[KIND == 2 ? MAX_M : 1][8];  // silu(gate) * up (SWIGLU)
+  uint4 a[KIND == 2 ? 1 : MT];     // x (NONE, RMSNORM)
+  float v[KIND == 2 ? MT : 1][8];  // silu(gate) * up (SWIGLU)
   float4 g0, g1;                      // gamma (RMSNORM)
 
   __device__ __forceinline__ void load_gamma(const FwdParams& p, int64_t k) {
@@ -141,7 +142,7 @@ struct ActSlice {
       // 4..7) and each row is converted in place, so raw and converted rows
       // never need separate registers
 #pragma unroll
-      for (int m = 0; m < MAX_M; m++) {
+      for (int m = 0; m < MT; m++) {
         if (m < M) {
           const uint4 gq = __ldcg(reinterpret_cast<const uint4*>(p.gate + (int64_t)m * p.K + k));
           const uint4 uq = __ldcg(reinterpret_cast<const uint4*>(p.up + (int64_t)m * p.K + k));
@@ -152,7 +153,7 @@ struct ActSlice {
         }
       }
 #pragma unroll
-      for (int m = 0; m < MAX_M; m++) {
+      for (int m = 0; m < MT; m++) {
         if (m < M) {
           const uint4 gq = make_uint4(__float_as_uint(v[m][0]), __float_as_uint(v[m][1]), __float_as_uint(v[m][2]),
                                       __float_as_uint(v[m][3]));
@@ -167,7 +168,7 @@ struct ActSlice {
       }
     } else {
 #pragma unroll
-      for (int m = 0; m < MAX_M; m++)
+      for (int m = 0; m < MT; m++)
         if (m < M) a[m] = __ldcg(reinterpret_cast<const uint4*>(p.x + (int64_t)m * p.K + k));
     }
   }
@@ -533,24 +534,24 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   // Phases 1 and 2 are specialised per prologue kind: the kind is a launch
   // parameter (uniform across the grid), so one kernel serves every kind and
   // consecutive launches of different prologues run the same main loop code.
-  auto prologue = [&](auto kind_tag) {
-    constexpr int KIND = decltype(kind_tag)::value;
-    ActSlice<KIND> act;
+  auto prologue = [&](auto kind_tag, auto rows_tag) {
+    constexpr int KIND = decltype(kind_tag)::value, MT = decltype(rows_tag)::value;
+    ActSlice<KIND, MT> act;
     if (tid < n8) act.load_gamma(p, k_lo + tid * 8);  // a model parameter: may be read early
     pdl_wait();  // activations may be written by the previous kernel in the stream
 
     // ---- phase 1: prologue statistics of this CTA's K range, per row
     {
-      float amax[MAX_M], ssq[MAX_M];
+      float amax[MT], ssq[MT];
   #pragma unroll
-      for (int m = 0; m < MAX_M; m++) amax[m] = ssq[m] = 0.f;
+      for (int m = 0; m < MT; m++) amax[m] = ssq[m] = 0.f;
       for (int r = 0; r < rounds; r++) {
         const int64_t i8 = (int64_t)r * CONSUMERS + tid;
         if (i8 < n8) {
           if (r > 0) act.load_gamma(p, k_lo + i8 * 8);
           act.load(p, M, k_lo + i8 * 8);
   #pragma unroll
-          for (int m = 0; m < MAX_M; m++) {
+          for (int m = 0; m < MT; m++) {
             if (m < M) {
               float v[8];
               act.value(m, v, ssq[m]);
@@ -561,7 +562,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         }
       }
   #pragma unroll
-      for (int m = 0; m < MAX_M; m++) {
+      for (int m = 0; m < MT; m++) {
         if (m < M) {
           const float a = warp_max(amax[m]);
           const float q = KIND == 1 ? warp_sum(ssq[m]) : 0.f;
@@ -631,9 +632,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         const int kin = (int)(kl - jl * KB);
         uint8_t* blk = bop + jl * p.bbf;
         const int pr = kin / PAIR_K, step = (kin / KSTEP) & 1, half = (kin % KSTEP) >= 8;
-        float rowsum[MAX_M], rowlo[MAX_M];  // rowlo: k 0..3 of the 8 (groups of 4)
+        float rowsum[MT], rowlo[MT];  // rowlo: k 0..3 of the 8 (groups of 4)
   #pragma unroll
-        for (int m = 0; m < MAX_M; m++) {
+        for (int m = 0; m < MT; m++) {
           rowsum[m] = 0.f;
           rowlo[m] = 0.f;
           if (inb && m < M) {
@@ -693,7 +694,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         // lanes [SEG*i, SEG*(i+1)) hold one sub-group's 8-k slices; lane bit 1
         // is the k-step, so summing over the other bits gives each chain's sum
   #pragma unroll
-        for (int m = 0; m < MAX_M; m++) {
+        for (int m = 0; m < MT; m++) {
           if (m < M) {  // M is the same in every lane
   #pragma unroll
             for (int o = 1; o < SEG; o <<= 1)
@@ -714,12 +715,28 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       }
     }
   };
+  // ... and for the rows of the launch (at most 1, 2, 4 or 8): the
+  // activation slice, the row loops and their registers then cover only the
+  // rows there are.
+  auto by_rows = [&](auto kind_tag) {
+    // (the order of the cases sets the code layout, which measurably matters:
+    // this one measured best for 1 and 8 rows together)
+    if (M > 4) {
+      prologue(kind_tag, KindTag<8>{});
+    } else if (M <= 1) {
+      prologue(kind_tag, KindTag<1>{});
+    } else if (M > 2) {
+      prologue(kind_tag, KindTag<4>{});
+    } else {
+      prologue(kind_tag, KindTag<2>{});
+    }
+  };
   if (p.kind == 0) {
-    prologue(KindTag<0>{});
+    by_rows(KindTag<0>{});
   } else if (p.kind == 1) {
-    prologue(KindTag<1>{});
+    by_rows(KindTag<1>{});
   } else {
-    prologue(KindTag<2>{});
+    by_rows(KindTag<2>{});
   }
   consumer_bar();
 

@@ -4,20 +4,20 @@
 // for expert banks (mode 1), and 4-bit codes with G >= 32 for codebook
 // levels (mode 2).  The prologue kind is a runtime
 // parameter, so consecutive launches of different prologues run the same
-// code.  The variants are instantiated in four translation units (compiled
+// code.  The variants are instantiated in seven translation units (compiled
 // in parallel) and declared extern where the host code takes their addresses.
 #pragma once
 
 #define QLIN_KERNELS_W4(X) X(4, 4, 0) X(4, 8, 0) X(4, 16, 0) X(4, 32, 0) X(4, 64, 0) X(4, 128, 0) X(4, 256, 0)
-#define QLIN_KERNELS_W6_CODEBOOK(X)                                                                        \
-  X(6, 16, 0) X(6, 32, 0) X(6, 64, 0) X(6, 128, 0) X(6, 256, 0)                                             \
-  X(4, 32, 2) X(4, 64, 2) X(4, 128, 2) X(4, 256, 2)
-#define QLIN_KERNELS_MOE(X)                                                                                \
-  X(4, 32, 1) X(4, 64, 1) X(4, 128, 1) X(4, 256, 1) X(6, 32, 1) X(6, 64, 1) X(6, 128, 1) X(6, 256, 1)
-#define QLIN_KERNELS_EXPORT(X)                                                                             \
-  X(4, 4, 3) X(4, 8, 3) X(4, 16, 3) X(4, 32, 3) X(4, 64, 3) X(4, 128, 3) X(4, 256, 3)                       \
-  X(6, 16, 3) X(6, 32, 3) X(6, 64, 3) X(6, 128, 3) X(6, 256, 3)
-#define QLIN_KERNELS_ALL(X) QLIN_KERNELS_W4(X) QLIN_KERNELS_W6_CODEBOOK(X) QLIN_KERNELS_MOE(X) QLIN_KERNELS_EXPORT(X)
+#define QLIN_KERNELS_W6(X) X(6, 16, 0) X(6, 32, 0) X(6, 64, 0) X(6, 128, 0) X(6, 256, 0)
+#define QLIN_KERNELS_CODEBOOK(X) X(4, 32, 2) X(4, 64, 2) X(4, 128, 2) X(4, 256, 2)
+#define QLIN_KERNELS_MOE_W4(X) X(4, 32, 1) X(4, 64, 1) X(4, 128, 1) X(4, 256, 1)
+#define QLIN_KERNELS_MOE_W6(X) X(6, 32, 1) X(6, 64, 1) X(6, 128, 1) X(6, 256, 1)
+#define QLIN_KERNELS_EXPORT_W4(X) X(4, 4, 3) X(4, 8, 3) X(4, 16, 3) X(4, 32, 3) X(4, 64, 3) X(4, 128, 3) X(4, 256, 3)
+#define QLIN_KERNELS_EXPORT_W6(X) X(6, 16, 3) X(6, 32, 3) X(6, 64, 3) X(6, 128, 3) X(6, 256, 3)
+#define QLIN_KERNELS_ALL(X)                                                                                 \
+  QLIN_KERNELS_W4(X) QLIN_KERNELS_W6(X) QLIN_KERNELS_CODEBOOK(X) QLIN_KERNELS_MOE_W4(X) QLIN_KERNELS_MOE_W6(X) \
+  QLIN_KERNELS_EXPORT_W4(X) QLIN_KERNELS_EXPORT_W6(X)
 
 #define QLIN_INSTANTIATE(B, G, M) template __global__ void qlin::qlin_forward_kernel<B, G, M>(qlin::FwdParams);
 #define QLIN_DECLARE_EXTERN(B, G, M) \

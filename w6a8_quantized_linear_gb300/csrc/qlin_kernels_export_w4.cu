@@ -1,0 +1,5 @@
+// Forward-kernel variants: 4-bit codes with the test hooks (see qlin_instances.h).
+#include "qlin_forward.cuh"
+#include "qlin_instances.h"
+
+QLIN_KERNELS_EXPORT_W4(QLIN_INSTANTIATE)

@@ -1,0 +1,5 @@
+// Forward-kernel variants: expert banks of 6-bit codes (see qlin_instances.h).
+#include "qlin_forward.cuh"
+#include "qlin_instances.h"
+
+QLIN_KERNELS_MOE_W6(QLIN_INSTANTIATE)
