@@ -379,13 +379,13 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     // expert has no work, and its whole cluster (same blockIdx.y) leaves
     // here, before any barrier or shared-memory exchange.
     pdl_wait();
+    const int nid = p.M * p.topk;
+    const int my_id = tid < nid ? p.ids[tid] : -1;  // in flight while the bitmap is cleared
     for (int w = tid; w < MOE_MAX_E / 32; w += GEMV_THREADS) s_ebits[w] = 0u;
     if (tid == 0) s_expert = -1;
+    if (tid < MAX_M) s_tokmask[tid] = 0u;
     __syncthreads();
-    if (tid < p.M * p.topk) {
-      const int e = p.ids[tid];
-      if (e >= 0 && e < p.E) atomicOr(&s_ebits[e >> 5], 1u << (e & 31));
-    }
+    if (my_id >= 0 && my_id < p.E) atomicOr(&s_ebits[my_id >> 5], 1u << (my_id & 31));
     __syncthreads();
     if (warp == 0) {
       constexpr int WPL = MOE_MAX_E / 32 / 32;  // bitmap words per lane
@@ -420,12 +420,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     __syncthreads();
     const int expert = s_expert;
     if (expert < 0) return;
-    if (tid < p.M) {
-      uint32_t mask = 0;
-      for (int j = 0; j < p.topk; j++)
-        if (p.ids[tid * p.topk + j] == expert) mask |= 1u << j;
-      s_tokmask[tid] = mask;
-    }
+    // the slots of each token routed here, from the ids already in registers
+    // (visible to every thread after the barrier initialisation's __syncthreads)
+    if (tid < nid && my_id == expert) atomicOr(&s_tokmask[tid / p.topk], 1u << (tid % p.topk));
     packed = p.bank + (int64_t)expert * (p.ne / TILE_N) * p.tile_full;
     y = p.ymoe;
     bias = p.bank_bias ? p.bank_bias + (int64_t)expert * p.ne : nullptr;
