@@ -127,6 +127,12 @@ def barrier(ws):
         dist.barrier()
 
 
+def job_gbs(world: int, bytes_per_rank: int, ms: float) -> float:
+    """Whole-job throughput of N replicas: every rank streams bytes_per_rank
+    per step, and the step takes the slowest rank's time (ms, max over ranks)."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def max_over_ranks(v: float, ws: int, device) -> float:
     if ws == 1:
         return v
@@ -512,8 +518,8 @@ def main():
     clocks = clk.summary()
     t1 = max_over_ranks(t1, world, dev)
     t8 = max_over_ranks(t8, world, dev)
-    gbs1 = world * wb / (t1 * 1e-3) / 1e9
-    gbs8 = world * wb / (t8 * 1e-3) / 1e9
+    gbs1 = job_gbs(world, wb, t1)
+    gbs8 = job_gbs(world, wb, t8)
     ts1 = time_graph(s1, stream, max(3, args.steps // 2), 3)
     ts8 = time_graph(s8, stream, max(3, args.steps // 2), 3)
 
@@ -555,7 +561,7 @@ def main():
         e1.record(stream)
     torch.cuda.synchronize()
     te2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
-    gbs_e2e = world * wb / (te2e * 1e-3) / 1e9
+    gbs_e2e = job_gbs(world, wb, te2e)
 
     assert qlin.read_device_status(stack.ws) == qlin.OK
 
@@ -586,8 +592,8 @@ def main():
         "pct_of_8tbs_spec": 100.0 * gbs1 / world / 8000.0,
         "m8": {"value": gbs8, "ms_per_step": t8, "pct_of_hbm_peak": 100.0 * gbs8 / world / peak},
         "t8_over_t1": t8 / t1,
-        "separate_launches": {"launches_per_step": ncalls_sep, "value": world * wb / (ts1 * 1e-3) / 1e9,
-                              "ms_per_step": ts1, "m8": world * wb / (ts8 * 1e-3) / 1e9, "t8_over_t1": ts8 / ts1},
+        "separate_launches": {"launches_per_step": ncalls_sep, "value": job_gbs(world, wb, ts1),
+                              "ms_per_step": ts1, "m8": job_gbs(world, wb, ts8), "t8_over_t1": ts8 / ts1},
         "per_group": per,
         "widened_paths": widened,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
