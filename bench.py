@@ -149,7 +149,7 @@ def max_over_ranks(v: float, ws: int, device) -> float:
 # kernel reports no traffic until it is captured again.
 KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
 TRAFFIC = {
-    "f9abac9b6e2dc4ab": {"bytes_per_launch": 97588992,
+    "04b1241c318ed1dd": {"bytes_per_launch": 97608704,
                          "source": "profiles/forward_gate_up_w4a8_k5120.md (ncu --set full, one gate/up launch)"},
 }
 
