@@ -334,6 +334,72 @@ def next_rows(stack, stream, iters: int, peak: float):
     return out
 
 
+def config_lines(device, stream, iters: int, peak: float):
+    """Each single-linear benchmark configuration (4096 x 4096 RMSNorm, the
+    12288 -> 4096 SwiGLU down projection, and the two W6A8 G=32 shapes) at
+    M = 1 and 8: one launch per weight, over enough distinct weights that
+    they exceed L2 (the inputs are not L2-resident), in one graph."""
+    import torch
+
+    from w6a8_quantized_linear_gb300 import inputs, qlin
+    out = {}
+    g = torch.Generator(device=device)
+    g.manual_seed(11)
+    for name in ("c2_w4a8_rmsnorm", "c3_w4a8_swiglu", "c4_w6a8_up", "c4_w6a8_down"):
+        cfg = inputs.CONFIGS[name]
+        fmt, kind, N, K, G = cfg["fmt"], cfg["kind"], cfg["N"], cfg["K"], cfg["G"]
+        lo, hi = cfg["scale_range"]
+        nbytes = qlin.packed_bytes(fmt, N, K, G)
+        copies = max(2, -(-(256 << 20) // nbytes))  # at least 256 MB of weights per pass
+        ncb = nbytes - N * (K // G) * 4
+        rws = torch.empty(qlin.repack_workspace_bytes(fmt, N, K, G)[1], dtype=torch.uint8, device=device)
+        weights = []
+        for _ in range(copies):
+            w = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            w[:ncb] = torch.randint(0, 256, (ncb,), generator=g, dtype=torch.uint8, device=device)
+            w[ncb:].view(torch.float32).uniform_(lo, hi, generator=g)
+            qlin.repack(w, fmt, N, K, G, ws=rws)
+            weights.append(w)
+        del rws
+        ws = qlin.new_workspace(qlin.forward_workspace_bytes(fmt, N, K, G), device)
+        line = {"fmt": fmt, "prologue": kind, "N": N, "K": K, "G": G, "weight_bytes": nbytes, "weights": copies}
+        t = {}
+        for M in (1, 8):
+            x = gate = up = gamma = None
+            if kind == "swiglu":
+                gate = torch.randn(M, K, generator=g, device=device).to(torch.bfloat16)
+                up = torch.randn(M, K, generator=g, device=device).to(torch.bfloat16)
+            else:
+                x = torch.randn(M, K, generator=g, device=device).to(torch.bfloat16)
+            if kind == "rmsnorm":
+                gamma = torch.empty(K, device=device).uniform_(0.5, 1.5, generator=g)
+            y = torch.empty(M, N, device=device)
+
+            def call(w):
+                qlin.forward(fmt, kind, w, N, K, G, x=x, gate=gate, up=up, gamma=gamma, y=y, ws=ws,
+                             flags=qlin.FLAG_PDL, stream=stream)
+            call(weights[0])
+            torch.cuda.synchronize(device)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(gr, stream=stream):
+                    for _ in range(4):
+                        for w in weights:
+                            call(w)
+            ms = time_graph(gr, stream, iters, 3)
+            us = ms * 1e3 / (4 * copies)
+            t[M] = us
+            line[f"m{M}"] = {"us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
+                             "frac_of_measured_hbm": nbytes / (us * 1e-6) / 1e9 / peak}
+            del gr
+        line["t8_over_t1"] = t[8] / t[1]
+        assert qlin.read_device_status(ws) == qlin.OK
+        out[name] = line
+        del weights
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_graph(g, stream, iters: int, warmup: int, ws_world=1, device=None):
     import torch
     for _ in range(warmup):
@@ -536,6 +602,7 @@ def main():
             del g
 
     widened = next_rows(stack, stream, max(3, args.steps // 2), peak)
+    per_config = config_lines(dev, stream, max(3, args.steps // 4), peak)
 
     # end to end through the public call with host buffers: pinned host
     # activations in, every call's output back, each step
@@ -596,6 +663,7 @@ def main():
                               "ms_per_step": ts1, "m8": job_gbs(world, wb, ts8), "t8_over_t1": ts8 / ts1},
         "per_group": per,
         "widened_paths": widened,
+        "per_config": per_config,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic["bytes_per_launch"] if traffic else None,
                      "kernel": "qlin_forward_kernel<4,128,0> (RMSNorm prologue): the gate/up multi-weight launch, M=1, "
