@@ -273,7 +273,9 @@ qlin_status qlin_read_device_status(const void* ws, void* stream);
  * Test export: qlin_forward with extra outputs (device pointers, each may be
  * NULL): y fp32 [M, N]; acc int32 [M, N, K/G], the exact per-group integer
  * sums sum_k q[m,k] * level[n,k]; q int8 [M, K], the activation codes; s fp32
- * [M], the row scales.
+ * [M], the row scales.  It runs a build of the forward kernel that carries
+ * these exports (the production kernels do not), with the same arithmetic:
+ * its y equals qlin_forward's bit for bit.
  */
 qlin_status qlin_debug_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
                                const void* packed, const void* x, const void* gate, const void* up,
@@ -295,7 +297,7 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
                                      int64_t unit, void* stream);
 
 /*
- * qlin_forward without a caller workspace.  The paper has no counterpart: this
+ * qlin_forward without a caller workspace.  The method has no counterpart: this
  * is for callers that cannot allocate device memory where they run the layer
  * (a host whose memory pool owns the whole device and forbids cudaMalloc, code
  * that must avoid cudaMalloc's implicit synchronisation, a fixed-footprint
