@@ -535,6 +535,54 @@ def run_linear(args):
     return 0
 
 
+def run_profile_case(args):
+    """C launches of one benchmark configuration (--config NAME), or of the
+    expert-bank launch on a stack gate weight read as 17 experts x 1024 rows
+    (--moe, 8 routed experts per token), on distinct weights; for profilers."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from w6a8_quantized_linear_gb300 import inputs, qlin
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    if args.moe:
+        fmt, kind, (lo, hi), G = "w4a8", "rmsnorm", inputs.STACK_SCALES, inputs.STACK_G
+        K, N, E, NE = 5120, 17408, 17, 1024
+    else:
+        cfg = inputs.CONFIGS[args.config]
+        fmt, kind, N, K, G, (lo, hi) = cfg["fmt"], cfg["kind"], cfg["N"], cfg["K"], cfg["G"], cfg["scale_range"]
+    nbytes = qlin.packed_bytes(fmt, N, K, G)
+    ncb = nbytes - N * (K // G) * 4
+    ws = qlin.new_workspace(qlin.forward_workspace_bytes(fmt, N, K, G), dev)
+    x = gate = up = gamma = None
+    if kind == "swiglu":
+        gate = torch.randn(args.M, K, generator=g, device=dev).to(torch.bfloat16)
+        up = torch.randn(args.M, K, generator=g, device=dev).to(torch.bfloat16)
+    else:
+        x = torch.randn(args.M, K, generator=g, device=dev).to(torch.bfloat16)
+    if kind == "rmsnorm":
+        gamma = torch.empty(K, device=dev).uniform_(0.5, 1.5, generator=g)
+    gen = torch.Generator().manual_seed(3)
+    for _ in range(args.calls):
+        w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        w[:ncb] = torch.randint(0, 256, (ncb,), generator=g, dtype=torch.uint8, device=dev)
+        w[ncb:].view(torch.float32).uniform_(lo, hi, generator=g)
+        qlin.repack(w, fmt, N, K, G)
+        if args.moe:
+            ids = torch.stack([torch.randperm(E, generator=gen)[:8] for _ in range(args.M)]).to(torch.int32).to(dev)
+            qlin.forward_moe(fmt, kind, w, E, NE, K, G, ids, x=x, gamma=gamma, ws=ws, flags=qlin.FLAG_PDL)
+        else:
+            qlin.forward(fmt, kind, w, N, K, G, x=x, gate=gate, up=up, gamma=gamma, ws=ws, flags=qlin.FLAG_PDL)
+    torch.cuda.synchronize()
+    assert qlin.read_device_status(ws) == qlin.OK
+    print(json.dumps({"case": "moe" if args.moe else args.config, "M": args.M, "N": N, "K": K, "G": G,
+                      "calls": args.calls, "bytes_per_launch": nbytes * 8 // 17 if args.moe else nbytes}))
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -548,12 +596,16 @@ def main():
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--codebook", action="store_true", help="profile mode: levels from a 16-entry codebook")
+    ap.add_argument("--config", default=None, help="profile mode: one single-linear benchmark configuration")
+    ap.add_argument("--moe", action="store_true", help="profile mode: the expert-bank launch")
     ap.add_argument("--print-kernel-hash", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.linear is not None:
         return run_linear(args)
+    if args.config is not None or args.moe:
+        return run_profile_case(args)
     if args.print_kernel_hash:
         print(kernel_hash())
         return 0

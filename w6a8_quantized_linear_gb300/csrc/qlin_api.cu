@@ -194,7 +194,9 @@ qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int m
     pl.C = (int)c;
     pl.upc = (int)((g.J + c - 1) / c);
     const int64_t extra = mode == 2 ? CODEBOOK_LUT_BYTES : 0;
-    if (!(carve(g, bbf, pl, SMEM_TWO_PER_SM, 3, extra) || carve(g, bbf, pl, SMEM_MAX, 2, extra))) continue;
+    // two CTAs per SM need at least two stages each (four units in flight per
+    // SM keep DRAM busy); with fewer, one CTA per SM gets the whole budget
+    if (!(carve(g, bbf, pl, SMEM_TWO_PER_SM, 2, extra) || carve(g, bbf, pl, SMEM_MAX, 2, extra))) continue;
     const int n = active_clusters(dc, fn, pl.C, pl.smem);
     if (n < 1) continue;
     const int64_t cost = (NB + n - 1) / n * pl.upc;
