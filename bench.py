@@ -337,8 +337,10 @@ def next_rows(stack, stream, iters: int, peak: float):
 def config_lines(device, stream, iters: int, peak: float):
     """Each single-linear benchmark configuration (4096 x 4096 RMSNorm, the
     12288 -> 4096 SwiGLU down projection, and the two W6A8 G=32 shapes) at
-    M = 1 and 8: one launch per weight, over enough distinct weights that
-    they exceed L2 (the inputs are not L2-resident), in one graph."""
+    every M the configuration names (1, 2, 4, 8 or 1..8): one launch per
+    weight, over enough distinct weights that they exceed L2 (the inputs are
+    not L2-resident), in one graph.  M = 1 and 8 in full, the others as
+    microseconds per launch."""
     import torch
 
     from w6a8_quantized_linear_gb300 import inputs, qlin
@@ -364,7 +366,7 @@ def config_lines(device, stream, iters: int, peak: float):
         ws = qlin.new_workspace(qlin.forward_workspace_bytes(fmt, N, K, G), device)
         line = {"fmt": fmt, "prologue": kind, "N": N, "K": K, "G": G, "weight_bytes": nbytes, "weights": copies}
         t = {}
-        for M in (1, 8):
+        for M in cfg["Ms"]:
             x = gate = up = gamma = None
             if kind == "swiglu":
                 gate = torch.randn(M, K, generator=g, device=device).to(torch.bfloat16)
@@ -389,9 +391,11 @@ def config_lines(device, stream, iters: int, peak: float):
             ms = time_graph(gr, stream, iters, 3)
             us = ms * 1e3 / (4 * copies)
             t[M] = us
-            line[f"m{M}"] = {"us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
-                             "frac_of_measured_hbm": nbytes / (us * 1e-6) / 1e9 / peak}
+            if M in (1, 8):
+                line[f"m{M}"] = {"us_per_launch": us, "GB/s": nbytes / (us * 1e-6) / 1e9,
+                                 "frac_of_measured_hbm": nbytes / (us * 1e-6) / 1e9 / peak}
             del gr
+        line["us_per_launch_by_M"] = {str(M): round(v, 3) for M, v in t.items()}
         line["t8_over_t1"] = t[8] / t[1]
         assert qlin.read_device_status(ws) == qlin.OK
         out[name] = line
