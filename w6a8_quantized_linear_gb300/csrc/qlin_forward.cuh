@@ -111,19 +111,19 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 r, float (&v)[8]) {
   }
 }
 
-// The activation slice of one thread: 8 consecutive k of every row.  All
-// loads are issued before any is used.  Activations are read through L2 (the
-// previous kernel in the stream may have written them); gamma, a parameter of
-// the model like the weights, is loaded separately (possibly before that
-// kernel completes, under QLIN_FLAG_PDL).  SwiGLU values are computed once, at
-// load, and kept in fp32.
+// A compile-time integer as a value (to pick a specialisation of a generic
+// lambda).
 template <int K>
-struct KindTag {
+struct IntTag {
   static constexpr int value = K;
 };
 
-// One thread's 8-wide K slice of every row, for prologue kind KIND and at
-// most MT rows.
+// The activation slice of one thread: 8 consecutive k of every row (at most
+// MT rows), for prologue kind KIND.  All loads are issued before any is used.
+// Activations are read through L2 (the previous kernel in the stream may have
+// written them); gamma, a parameter of the model like the weights, is loaded
+// separately (possibly before that kernel completes, under QLIN_FLAG_PDL).
+// SwiGLU values are computed once, at load, and kept in fp32.
 template <int KIND, int MT>
 struct ActSlice {
   uint4 a[KIND == 2 ? 1 : MT];     // x (NONE, RMSNORM)
@@ -719,21 +719,21 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     // (the order of the cases sets the code layout, which measurably matters:
     // this one measured best for 1 and 8 rows together)
     if (M > 4) {
-      prologue(kind_tag, KindTag<8>{});
+      prologue(kind_tag, IntTag<8>{});
     } else if (M <= 1) {
-      prologue(kind_tag, KindTag<1>{});
+      prologue(kind_tag, IntTag<1>{});
     } else if (M > 2) {
-      prologue(kind_tag, KindTag<4>{});
+      prologue(kind_tag, IntTag<4>{});
     } else {
-      prologue(kind_tag, KindTag<2>{});
+      prologue(kind_tag, IntTag<2>{});
     }
   };
   if (p.kind == 0) {
-    by_rows(KindTag<0>{});
+    by_rows(IntTag<0>{});
   } else if (p.kind == 1) {
-    by_rows(KindTag<1>{});
+    by_rows(IntTag<1>{});
   } else {
-    by_rows(KindTag<2>{});
+    by_rows(IntTag<2>{});
   }
   consumer_bar();
 
