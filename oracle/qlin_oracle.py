@@ -354,7 +354,7 @@ def _slab_pair_index():
     return np.broadcast_to(row, (32, 2, 4, 2)), np.broadcast_to(kk, (32, 2, 4, 2))
 
 
-def unpack_stream(fmt: str, N: int, K: int, G: int, buf) -> tuple[np.ndarray, np.ndarray]:
+def unpack_stream(fmt: str, N: int, K: int, G: int, buf, layout: str = "plain") -> tuple[np.ndarray, np.ndarray]:
     """Read codes [N, K] and scales [N, K/G] back out of the stream layout.
 
     The layout (documented with the repack entry point) is, in words:
@@ -368,7 +368,13 @@ def unpack_stream(fmt: str, N: int, K: int, G: int, buf) -> tuple[np.ndarray, np
     4i..4i+3 and 16+4i..16+4i+3 (low 4 bits of the code).  In the 2-bit plane
     word the top 2 bits of register i of step s (0 = A, 1 = B) sit at bits
     8s + 2*(i // 2) + 4*(i % 2) and 16 more than that.
+
+    ``layout="codebook"`` (4-bit codes whose levels come from a codebook) is
+    the same stream except inside a plane word: A-register i's two elements
+    sit in byte i, the even k at bits 8i..8i+3 and the odd k at 8i+4..8i+7.
     """
+    assert layout in ("plain", "codebook")
+    assert layout == "plain" or fmt == "w4a8", "only 4-bit codes have the codebook layout"
     b = BITS[fmt]
     buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
     assert N % 16 == 0 and K % 32 == 0 and K % G == 0
@@ -378,6 +384,8 @@ def unpack_stream(fmt: str, N: int, K: int, G: int, buf) -> tuple[np.ndarray, np
     elem = np.arange(2)[None, None, None, :]
     step = np.arange(2)[None, :, None, None]
     nib_shift = (16 * elem + 4 * reg).astype(np.uint32)                 # [1,1,4,2]
+    if layout == "codebook":
+        nib_shift = (8 * reg + 4 * elem).astype(np.uint32)
     hi_shift = (8 * step + 16 * elem + 2 * (reg // 2) + 4 * (reg % 2)).astype(np.uint32)  # [1,2,4,2]
     codes = np.full((N, K), -1, dtype=np.int64)
     sw = np.full((N, K // G), np.nan, dtype=np.float32)

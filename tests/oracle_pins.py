@@ -301,6 +301,35 @@ def check_stream_bijection(O):
             assert not np.intersect1d(src, hsrc).size, "2-bit plane shares bytes with the 4-bit plane"
 
 
+def check_stream_positions_codebook(O):
+    """The codebook layout: single codes at hand-derived positions, and every
+    code read from its own field (bijection), ragged tile and several units
+    included."""
+    g = read_golden("stream_positions_codebook.txt")
+    N, K, G = 16, 32, 32
+    size = O.file_bytes("w4a8", N, K, G)
+    for key in ("0", "9", "3", "15"):
+        for rest in g[key]:
+            n, k, nb, ns = int(key), int(rest[0]), int(rest[1]), int(rest[2])
+            buf = np.zeros(size, dtype=np.uint8)
+            buf[nb] = 0x5 << ns
+            codes, _ = O.unpack_stream("w4a8", N, K, G, buf, layout="codebook")
+            want = np.zeros((N, K), dtype=np.int64)
+            want[n, k] = 5
+            assert np.array_equal(codes, want), (n, k, np.argwhere(codes))
+    for N, K, G in ((144, 160, 32), (32, 256, 256)):
+        size = O.file_bytes("w4a8", N, K, G)
+        p = np.arange(size)
+        src = np.zeros((N, K), dtype=np.int64)
+        for j in range(4):
+            d = ((p >> (4 * j)) & 0xF).astype(np.uint8)
+            codes, _ = O.unpack_stream("w4a8", N, K, G, d | (d << 4), layout="codebook")
+            src |= (codes & 0xF) << (4 * j)
+        half, _ = O.unpack_stream("w4a8", N, K, G, np.full(size, 0x10, dtype=np.uint8), layout="codebook")
+        key = src * 2 + (half & 0xF)
+        assert np.unique(key).size == N * K
+
+
 def check_bias(O, seed=9):
     """A float bias is added once, unscaled, to every row: with every level zero
     y equals the bias exactly; sampled columns take the matching entries."""

@@ -35,12 +35,15 @@ MUTANTS = {
     "bias_dropped": ("y64 = y64 + (b if cols is None", "y64 = y64 + 0 * (b if cols is None"),
     "moe_expert_rows_offset": ("cols = e * N + sel", "cols = e * N + sel + (N if e == 0 else 0)"),
     "codebook_index_flipped": ("astype(np.float64)[np.asarray(codes)]", "astype(np.float64)[np.asarray(codes) ^ 8]"),
+    "codebook_layout_elements_swapped": ("nib_shift = (8 * reg + 4 * elem)", "nib_shift = (8 * reg + 4 * (1 - elem))"),
+    "codebook_layout_registers_as_plain": ("nib_shift = (8 * reg + 4 * elem)", "nib_shift = (16 * elem + 4 * reg)"),
     "bias_scaled_by_row_scale": ("y64 = y64 + (b if cols is None else b[np.asarray(cols)])[None, :]",
                                  "y64 = y64 + s[:, None] * (b if cols is None else b[np.asarray(cols)])[None, :]"),
 }
 
 PINS = ["hand_example", "file_layout", "forward_bruteforce", "quantize", "prologues",
-        "closed_forms", "invariants", "stream_positions", "stream_bijection", "bias", "moe", "codebook"]
+        "closed_forms", "invariants", "stream_positions", "stream_bijection", "stream_positions_codebook", "bias",
+        "moe", "codebook"]
 
 
 def build_mutant(old, new):
