@@ -279,12 +279,13 @@ class Stack:
 def next_rows(stack, stream, iters: int, peak: float):
     """The widened paths on the stack's gate weights (17408 x 5120, G = 128,
     RMSNorm prologue), 64 launches on 64 distinct weights in one graph each:
-    the single-weight launch, the same weights with a 16-level codebook, and
-    each weight read as an expert bank of 17 experts x 1024 rows (8 routed
-    experts for one token; 2 per token for 8 tokens)."""
+    the single-weight launch; 8 weights of the same shape in the codebook
+    stream layout with a 16-level codebook (378 MB, more than L2, eight
+    passes); and each stack weight read as an expert bank of 17 experts x
+    1024 rows (8 routed experts for one token; 2 per token for 8 tokens)."""
     import torch
 
-    from w6a8_quantized_linear_gb300 import qlin
+    from w6a8_quantized_linear_gb300 import inputs, qlin
     K, N = stack.shape["gate"]
     G = stack.G
     gen = torch.Generator().manual_seed(5)
@@ -298,6 +299,20 @@ def next_rows(stack, stream, iters: int, peak: float):
     weights = [row["gate"] for row in stack.weights]
     y = torch.empty(8 * N, device=stack.dev)
     wbytes = qlin.packed_bytes("w4a8", N, K, G)
+    # codebook weights: their own stream layout, 8 distinct weights (378 MB, more than L2)
+    lo, hi = inputs.STACK_SCALES
+    ncb = N * K // 2
+    rws = torch.empty(qlin.repack_workspace_bytes("w4a8", N, K, G)[1], dtype=torch.uint8, device=stack.dev)
+    gw = torch.Generator(device=stack.dev)
+    gw.manual_seed(6)
+    cb_weights = []
+    for _ in range(8):
+        w = torch.empty(wbytes, dtype=torch.uint8, device=stack.dev)
+        w[:ncb] = torch.randint(0, 256, (ncb,), generator=gw, dtype=torch.uint8, device=stack.dev)
+        w[ncb:].view(torch.float32).uniform_(lo, hi, generator=gw)
+        qlin.repack_codebook(w, N, K, G, ws=rws)
+        cb_weights.append(w)
+    del rws
 
     def plain(w):
         qlin.forward("w4a8", "rmsnorm", w, N, K, G, x=x1, gamma=gamma, y=y[:N].view(1, N), ws=stack.ws,
@@ -314,23 +329,28 @@ def next_rows(stack, stream, iters: int, peak: float):
                              flags=qlin.FLAG_PDL, stream=stream)
         return f
 
-    cases = [("single_weight", plain, wbytes), ("codebook", codebook, wbytes),
+    cases = [("single_weight", plain, wbytes), ("codebook", codebook, wbytes, cb_weights),
              ("moe_m1_top8", moe(ids1, x1), wbytes * 8 // E), ("moe_m8_top2", moe(ids8, x8),
                                                                 wbytes * len(set(ids8.flatten().tolist())) // E)]
     out = {}
-    for name, f, nbytes in cases:
-        f(weights[0])
+    for case in cases:
+        name, f, nbytes = case[:3]
+        ws_list = case[3] if len(case) > 3 else weights
+        f(ws_list[0])
         torch.cuda.synchronize(stack.dev)
+        reps = max(1, len(weights) // len(ws_list))
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
-                for w in weights:
-                    f(w)
+                for _ in range(reps):
+                    for w in ws_list:
+                        f(w)
         t = time_graph(g, stream, iters, 3)
-        us = t * 1e3 / len(weights)
+        us = t * 1e3 / (reps * len(ws_list))
         out[name] = {"us_per_launch": us, "weight_bytes_per_launch": nbytes, "GB/s": nbytes / (us * 1e-6) / 1e9,
                      "frac_of_measured_hbm": nbytes / (us * 1e-6) / 1e9 / peak}
         del g
+    del cb_weights
     return out
 
 
@@ -511,7 +531,10 @@ def run_linear(args):
             w = torch.empty(qlin.packed_bytes("w4a8", N, K, G), dtype=torch.uint8, device=dev)
             w[:ncb] = torch.randint(0, 256, (ncb,), generator=g, dtype=torch.uint8, device=dev)
             w[ncb:].view(torch.float32).uniform_(lo, hi, generator=g)
-            qlin.repack(w, "w4a8", N, K, G)
+            if args.codebook:
+                qlin.repack_codebook(w, N, K, G)
+            else:
+                qlin.repack(w, "w4a8", N, K, G)
             ws_.append(w)
         x = gate = up = gamma = None
         if kind == "swiglu":

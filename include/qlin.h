@@ -145,6 +145,17 @@ qlin_status qlin_repack(int fmt, int64_t N, int64_t K, int64_t G, void* buf,
  * forward keeps everything else (the quantised activations, the split-K
  * partial sums) in on-chip shared memory.
  */
+/*
+ * qlin_repack for a W4A8 weight whose levels come from a codebook
+ * (qlin_forward_codebook): the same stream, except that in a 4-bit plane
+ * word A-register i's two codes sit in byte i (even k at bits 8i..8i+3, odd
+ * k at 8i+4..8i+7), so that one table lookup yields one register.  Same
+ * arguments, sizes and errors as qlin_repack with fmt = QLIN_W4A8.  A buffer
+ * repacked this way is for qlin_forward_codebook only.
+ */
+qlin_status qlin_repack_codebook(int64_t N, int64_t K, int64_t G, void* buf, void* ws, size_t ws_bytes,
+                                 void* stream);
+
 qlin_status qlin_forward_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t G, size_t* bytes);
 qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
@@ -241,7 +252,8 @@ qlin_status qlin_forward_moe(int fmt, int prologue, int M, int E, int64_t N, int
  *   y[m][n] = s_m * sum_g sw[n][g] * sum_{k in g} q[m][k] * codebook[code[n][k]]
  *             (+ bias[n]).
  *   fmt      : QLIN_W4A8 only (else QLIN_ERR_INVALID_ARG); G >= 32 here.
- *   packed   : the repacked stream, as for qlin_forward (same repack).
+ *   packed   : the stream written by qlin_repack_codebook (the codebook
+ *              layout of the 4-bit plane), 16-byte aligned.
  *   codebook : device fp32 [16], 4-byte aligned.  It is read like `packed`
  *              (before the dependency wait under QLIN_FLAG_PDL).
  *   bias     : device fp32 [N], or NULL.

@@ -35,6 +35,14 @@ def _table(seed):
     return t / np.float32(np.abs(t).max())
 
 
+def _device_cb(c):
+    """The case on the GPU with its weight in the codebook stream layout."""
+    d = device_case(c)  # activations (and a plain-layout copy of the weight)
+    d["w_cb"] = c.wbuf.to(DEV)
+    qlin.repack_codebook(d["w_cb"], c.N, c.K, c.G)
+    return d
+
+
 def _oracle(c, cb, cols=None, bias=None):
     bits = (lambda t: inputs.bf16_bits(t) if t is not None else None)
     return O.forward(c.fmt, c.kind, c.N, c.K, c.G, c.wbuf.numpy(), x=bits(c.x), gate=bits(c.gate), up=bits(c.up),
@@ -43,7 +51,7 @@ def _oracle(c, cb, cols=None, bias=None):
 
 
 def _run(c, d, cb, bias=None, flags=qlin.FLAG_PDL):
-    return qlin.forward_codebook("w4a8", c.kind, d["w"], torch.from_numpy(np.ascontiguousarray(cb)).to(DEV), c.N,
+    return qlin.forward_codebook("w4a8", c.kind, d["w_cb"], torch.from_numpy(np.ascontiguousarray(cb)).to(DEV), c.N,
                                  c.K, c.G, x=d["x"], gate=d["gate"], up=d["up"], gamma=d["gamma"], eps=c.eps,
                                  bias=bias, flags=flags)
 
@@ -57,16 +65,30 @@ def _run(c, d, cb, bias=None, flags=qlin.FLAG_PDL):
 ])
 def test_codebook_matches_oracle(kind, M, N, K, G):
     c = inputs.make_case("w4a8", kind, M, N, K, G, seed=N + K + M)
-    d = device_case(c)
+    d = _device_cb(c)
     cb = _table(K + G)
     y = _run(c, d, cb)
     ref = _oracle(c, cb)
     assert_y_close(y.cpu().numpy(), ref["y64"], f"codebook {kind} M={M} N={N} K={K} G={G}")
 
 
+@pytest.mark.parametrize("N,K,G", [(144, 160, 32), (272, 1024, 128), (32, 512, 256)])
+def test_codebook_repack_round_trip(N, K, G):
+    """The codebook repack writes the oracle's codebook layout, byte for byte
+    in meaning: reading the GPU stream back gives the checkpoint's codes and
+    scales."""
+    c = inputs.make_case("w4a8", "none", 1, N, K, G, seed=N + K)
+    w = c.wbuf.to(DEV)
+    qlin.repack_codebook(w, N, K, G)
+    codes, sw = O.unpack_stream("w4a8", N, K, G, w.cpu().numpy(), layout="codebook")
+    want_codes, want_sw = O.unpack_file("w4a8", N, K, G, c.wbuf.numpy())
+    assert np.array_equal(codes, want_codes)
+    assert np.array_equal(sw, want_sw)
+
+
 def test_codebook_with_bias():
     c = inputs.make_case("w4a8", "swiglu", 4, 528, 1280, 64, seed=9)
-    d = device_case(c)
+    d = _device_cb(c)
     cb = _table(3) * np.float32(0.37)
     bias = (torch.randn(c.N, generator=torch.Generator().manual_seed(1)) * 3).float()
     y = _run(c, d, cb, bias=bias.to(DEV))
@@ -78,7 +100,7 @@ def test_uniform_codebook_equals_plain_levels():
     """The table code - 8 is the format's uniform levels: the oracle with that
     table equals the plain oracle, and the GPU codebook path matches both."""
     c = inputs.make_case("w4a8", "rmsnorm", 8, 784, 2048, 128, seed=21)
-    d = device_case(c)
+    d = _device_cb(c)
     uni = np.arange(16, dtype=np.float32) - 8
     y_cb = _run(c, d, uni).cpu().numpy()
     y_plain = qlin.forward("w4a8", c.kind, d["w"], c.N, c.K, c.G, x=d["x"], gamma=d["gamma"], eps=c.eps).cpu().numpy()
@@ -91,7 +113,7 @@ def test_power_of_two_table_scaling_is_exact():
     """The kernel normalises the table by a power of two: scaling the table by
     2^e scales y by exactly 2^e (no bias, no overflow)."""
     c = inputs.make_case("w4a8", "none", 2, 272, 1024, 64, seed=4)
-    d = device_case(c)
+    d = _device_cb(c)
     cb = _table(8)
     y0 = _run(c, d, cb)
     for e in (7, -9):
@@ -101,7 +123,7 @@ def test_power_of_two_table_scaling_is_exact():
 
 def test_zero_codebook_gives_bias():
     c = inputs.make_case("w4a8", "rmsnorm", 3, 144, 512, 32, seed=6)
-    d = device_case(c)
+    d = _device_cb(c)
     bias = torch.randn(c.N, generator=torch.Generator().manual_seed(2)).float()
     y = _run(c, d, np.zeros(16, np.float32), bias=bias.to(DEV))
     assert torch.equal(y.cpu(), bias.expand(3, -1))
@@ -110,7 +132,7 @@ def test_zero_codebook_gives_bias():
 @pytest.mark.parametrize("M", [1, 8])
 def test_codebook_full_size_sampled(M):
     c = inputs.config_case("c2_w4a8_rmsnorm", M, seed=M + 40)
-    d = device_case(c)
+    d = _device_cb(c)
     cb = _table(M)
     y = _run(c, d, cb)
     cols = sample_cols(c.N, 256, seed=M)

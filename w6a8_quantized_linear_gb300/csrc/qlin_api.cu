@@ -477,8 +477,9 @@ qlin_status qlin_repack_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t G
   return QLIN_OK;
 }
 
-qlin_status qlin_repack(int fmt, int64_t N, int64_t K, int64_t G, void* buf, void* ws, size_t ws_bytes,
-                        void* stream) {
+namespace {
+qlin_status repack_impl(int fmt, int64_t N, int64_t K, int64_t G, void* buf, void* ws, size_t ws_bytes,
+                        void* stream, bool cb_layout) {
   qlin_status st = check_shape_impl(fmt, N, K, G);
   if (st != QLIN_OK) return st;
   if (N == 0) return QLIN_OK;
@@ -506,6 +507,7 @@ qlin_status qlin_repack(int fmt, int64_t N, int64_t K, int64_t G, void* buf, voi
   rp.stage = w + sc;
   rp.scales = reinterpret_cast<const float*>(w);
   rp.bits = g.bits;
+  rp.cb_layout = cb_layout ? 1 : 0;
   rp.N = N;
   rp.K = K;
   rp.G = G;
@@ -527,6 +529,17 @@ qlin_status qlin_repack(int fmt, int64_t N, int64_t K, int64_t G, void* buf, voi
     hi = lo;
   }
   return QLIN_OK;
+}
+}  // namespace
+
+qlin_status qlin_repack(int fmt, int64_t N, int64_t K, int64_t G, void* buf, void* ws, size_t ws_bytes,
+                        void* stream) {
+  return repack_impl(fmt, N, K, G, buf, ws, ws_bytes, stream, false);
+}
+
+qlin_status qlin_repack_codebook(int64_t N, int64_t K, int64_t G, void* buf, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return repack_impl(QLIN_W4A8, N, K, G, buf, ws, ws_bytes, stream, true);
 }
 
 qlin_status qlin_forward_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t G, size_t* bytes) {

@@ -223,9 +223,9 @@ __device__ __forceinline__ void unpack_step(uint32_t w, uint32_t h01, uint32_t h
 // Codebook levels (4-bit codes).  The table holds, for every byte value e
 // (codes lo = e & 15 and hi = e >> 4), the fp16 pair (level(lo), level(hi)),
 // one copy per lane: entry e of lane l at byte 128 e + 4 l, so the 32 lookups
-// of a warp fall in 32 different banks.  Byte J of a plane word holds the
-// codes of registers 2J % 4.. at one k (nibbles 2J, 2J + 1); two byte lookups
-// and a byte permute give a register's two k.
+// of a warp fall in 32 different banks.  In the codebook stream layout byte J
+// of a plane word holds register J's two codes (even k low), so one lookup
+// is one A register.
 template <int J>
 __device__ __forceinline__ uint32_t lut_byte_off(uint32_t w, uint32_t lane4) {
   constexpr int s = 8 * J - 7;  // bits 8J..8J+7 to 7..14
@@ -235,14 +235,10 @@ __device__ __forceinline__ uint32_t lut_byte_off(uint32_t w, uint32_t lane4) {
   return r;
 }
 __device__ __forceinline__ void unpack_step_lut(uint32_t w, const uint8_t* lut, uint32_t lane4, uint32_t (&a)[4]) {
-  const uint32_t x0 = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<0>(w, lane4));  // nibbles 0, 1
-  const uint32_t x1 = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<1>(w, lane4));  // 2, 3
-  const uint32_t x2 = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<2>(w, lane4));  // 4, 5
-  const uint32_t x3 = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<3>(w, lane4));  // 6, 7
-  a[0] = __byte_perm(x0, x2, 0x5410);  // register i: nibbles i and 4 + i
-  a[1] = __byte_perm(x0, x2, 0x7632);
-  a[2] = __byte_perm(x1, x3, 0x5410);
-  a[3] = __byte_perm(x1, x3, 0x7632);
+  a[0] = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<0>(w, lane4));
+  a[1] = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<1>(w, lane4));
+  a[2] = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<2>(w, lane4));
+  a[3] = *reinterpret_cast<const uint32_t*>(lut + lut_byte_off<3>(w, lane4));
 }
 
 // One 32-wide k pair of one 16-row slab: step A into chain ca, step B into cb.

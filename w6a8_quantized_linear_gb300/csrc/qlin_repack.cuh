@@ -27,6 +27,7 @@ struct RepackParams {
   const uint8_t* stage;    // staged checkpoint codes of tiles [t_begin, t_end)
   const float* scales;     // all checkpoint scales [N, K/G]
   int bits;
+  int cb_layout;           // 4-bit codes for codebook levels: register i's two codes in byte i
   int64_t N, K, G, KB, J, tile_full, t_begin;
 };
 
@@ -70,7 +71,7 @@ __global__ void qlin_repack_write_kernel(RepackParams p) {
           for (int e = 0; e < 2; e++) {
             const int64_t r = slab * 16 + g + 8 * (reg & 1);
             const int64_t k = kbase + 16 * step + 2 * tq + 8 * (reg >> 1) + e;
-            out |= (staged_code<BITS>(tc, row_bytes, r, k) & 0xFu) << (16 * e + 4 * reg);
+            out |= (staged_code<BITS>(tc, row_bytes, r, k) & 0xFu) << (p.cb_layout ? 8 * reg + 4 * e : 16 * e + 4 * reg);
           }
       } else {  // 2-bit plane word of lane x - 64
         const int lane = (int)(x - 64), g = lane >> 2, tq = lane & 3;

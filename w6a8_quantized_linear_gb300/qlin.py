@@ -51,6 +51,7 @@ def lib() -> ctypes.CDLL:
                 "qlin_packed_bytes": (sz, [i32, i64, i64, i64]),
                 "qlin_repack_workspace_bytes": (st, [i32, i64, i64, i64, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
                 "qlin_repack": (st, [i32, i64, i64, i64, vp, vp, sz, vp]),
+                "qlin_repack_codebook": (st, [i64, i64, i64, vp, vp, sz, vp]),
                 "qlin_forward_workspace_bytes": (st, [i32, i64, i64, i64, ctypes.POINTER(sz)]),
                 "qlin_workspace_init": (st, [vp, sz, vp]),
                 "qlin_forward": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, sz,
@@ -137,6 +138,17 @@ def repack(buf: torch.Tensor, fmt, N: int, K: int, G: int, ws: torch.Tensor | No
         _, rec = repack_workspace_bytes(fmt, N, K, G)
         ws = torch.empty(rec, dtype=torch.uint8, device=buf.device)
     _check(lib().qlin_repack(_fmt(fmt), N, K, G, _ptr(buf), _ptr(ws), ws.numel(), _stream(stream)), "repack")
+    return buf
+
+
+def repack_codebook(buf: torch.Tensor, N: int, K: int, G: int, ws: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """``repack`` for a W4A8 weight used with a codebook (``forward_codebook``):
+    the codebook stream layout, in place."""
+    if ws is None:
+        _, rec = repack_workspace_bytes("w4a8", N, K, G)
+        ws = torch.empty(rec, dtype=torch.uint8, device=buf.device)
+    _check(lib().qlin_repack_codebook(N, K, G, _ptr(buf), _ptr(ws), ws.numel(), _stream(stream)), "repack_codebook")
     return buf
 
 
