@@ -130,6 +130,15 @@ def test_repack_rejects_bad_arguments(L):
     assert L.qlin_repack(0, 0, 256, 32, None, None, 0, None) == qlin.OK
 
 
+def test_repack_codebook_rejects_bad_arguments(L):
+    assert L.qlin_repack_codebook(512, 256, 32, None, 256, 1 << 20, None) == qlin.ERR_INVALID_ARG
+    assert L.qlin_repack_codebook(512, 256, 32, 8, 256, 1 << 20, None) == qlin.ERR_INVALID_ARG
+    assert L.qlin_repack_codebook(512, 256, 32, 256, 128, 1 << 20, None) == qlin.ERR_INVALID_ARG
+    assert L.qlin_repack_codebook(512, 256, 32, 256, 256, 16, None) == qlin.ERR_WORKSPACE
+    assert L.qlin_repack_codebook(512, 40, 8, 256, 256, 1 << 20, None) == qlin.ERR_INVALID_ARG
+    assert L.qlin_repack_codebook(0, 256, 32, None, None, 0, None) == qlin.OK
+
+
 def test_debug_fault_rejects_negative_unit(L):
     assert L.qlin_debug_forward_fault(0, 0, 1, 512, 256, 32, 256, 256, None, None, None, 1e-6, 256, 256, 1 << 20,
                                       -1, None) == qlin.ERR_INVALID_ARG
