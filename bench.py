@@ -149,7 +149,7 @@ def max_over_ranks(v: float, ws: int, device) -> float:
 # kernel reports no traffic until it is captured again.
 KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
 TRAFFIC = {
-    "04b1241c318ed1dd": {"bytes_per_launch": 97608704,
+    "82a3d2f54ef8ae1f": {"bytes_per_launch": 98126080,
                          "source": "profiles/forward_gate_up_w4a8_k5120.md (ncu --set full, one gate/up launch)"},
 }
 
