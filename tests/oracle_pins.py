@@ -396,3 +396,46 @@ def check_codebook(O, seed=11):
     yb = _bruteforce_y("w4a8", N, K, G, wbuf, r["q"], r["s"], codebook=cb)
     assert np.allclose(r["y64"], yb, rtol=1e-12, atol=1e-12 * np.abs(yb).max())
 
+
+
+def check_float_sanity(O, seed=12):
+    """The quantised result against the unquantised fp64 product of the
+    prologue output and the dequantised weight ("Comfy Quantization Formats",
+    section "Activations and smoothing": a backend without the integer kernel
+    dequantises and runs the float linear).  Everything on the float side is
+    computed independently of the oracle: the prologue with torch (rms_norm,
+    silu), the weight from the raw bytes through the bit-stream reader.  Per-row
+    symmetric int8 quantisation moves each activation by at most s_m / 2 with
+    s_m = amax_m / 127, so |y - y_float| <= s_m / 2 * sum_k |w[n, k]| exactly;
+    a wrong sign, offset, scale or prologue breaks the bound."""
+    rng = np.random.default_rng(seed)
+    for fmt in ("w4a8", "w6a8"):
+        b = {"w4a8": 4, "w6a8": 6}[fmt]
+        N, K, G = 16, 96, 32
+        codes = rng.integers(0, 1 << b, (N, K))
+        sw = rng.uniform(0.01, 0.02, (N, K // G)).astype(np.float32)
+        wbuf = O.pack_file(fmt, codes, sw)
+        raw = _bitstream_codes(fmt, N, K, wbuf) - (1 << (b - 1))
+        w = np.repeat(np.frombuffer(bytes(wbuf[N * K * b // 8:]), "<f4").reshape(N, K // G).astype(np.float64),
+                      G, axis=1) * raw
+        gen = torch.Generator().manual_seed(seed)
+        x = torch.randn(4, K, generator=gen).to(torch.bfloat16)
+        g = torch.randn(4, K, generator=gen).to(torch.bfloat16)
+        u = torch.randn(4, K, generator=gen).to(torch.bfloat16)
+        gamma = torch.empty(K).uniform_(0.5, 1.5, generator=gen)
+        cases = {
+            "none": (x.double(), dict(x=bits_of(x))),
+            "rmsnorm": (torch.nn.functional.rms_norm(x.double(), (K,), weight=gamma.double(), eps=1e-6),
+                        dict(x=bits_of(x), gamma=gamma.numpy(), eps=1e-6)),
+            "swiglu": (torch.nn.functional.silu(g.double()) * u.double(), dict(gate=bits_of(g), up=bits_of(u))),
+        }
+        for kind, (a, kw) in cases.items():
+            a = a.numpy()
+            r = O.forward(fmt, kind, N, K, G, wbuf, **kw)
+            yf = a @ w.T
+            s = np.abs(a).max(axis=1) / 127.0
+            bound = (s / 2.0)[:, None] * np.abs(w).sum(axis=1)[None, :]
+            err = np.abs(r["y64"] - yf)
+            assert np.all(err <= bound * (1 + 1e-9) + 1e-12), (fmt, kind, float((err / bound).max()))
+            # and the bound is not vacuous: the error is a small fraction of y
+            assert float(err.max()) < 0.05 * float(np.abs(yf).max()), (fmt, kind)

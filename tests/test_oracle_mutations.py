@@ -43,7 +43,7 @@ MUTANTS = {
 
 PINS = ["hand_example", "file_layout", "forward_bruteforce", "quantize", "prologues",
         "closed_forms", "invariants", "stream_positions", "stream_bijection", "stream_positions_codebook", "bias",
-        "moe", "codebook"]
+        "moe", "codebook", "float_sanity"]
 
 
 def build_mutant(old, new):
