@@ -729,7 +729,10 @@ def main():
     line = {
         "metric": METRIC, "value": gbs1, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t1, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "w4a8", "data": "synthetic",
+        "vs_baseline": None, "dtype": "int8",
+        "dtype_detail": "int8 activation codes x 4-bit weight levels, exact integer group sums (fp16 tensor-core "
+                        "MMA on exact integers, fp32 accumulate), fp32 group and row scales, fp32 output",
+        "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "layers": args.layers, "launches_per_step": ncalls,
                    "grouping": "q/k/v and gate/up as multi-weight launches sharing one prologue; o, down alone",
                    "weight_bytes_per_step": wb, "l2": "inputs larger than L2 (weights streamed once per step)",
