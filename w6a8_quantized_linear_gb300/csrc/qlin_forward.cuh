@@ -539,8 +539,14 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   // consecutive launches of different prologues run the same main loop code.
   auto prologue = [&](auto kind_tag, auto rows_tag) {
     constexpr int KIND = decltype(kind_tag)::value, MT = decltype(rows_tag)::value;
+    // Phase 1 runs its rounds last to first, so that the slice ends on round 0,
+    // which phase 2 then quantises without reading it again (not in the
+    // expert-bank mode, where the reversed loop measured slower).
+    constexpr bool REV = !MOE;
+    const int rl = REV ? rounds - 1 : 0;
     ActSlice<KIND, MT> act;
-    if (tid < n8) act.load_gamma(p, k_lo + tid * 8);  // a model parameter: may be read early
+    if (tid + (int64_t)rl * CONSUMERS < n8)
+      act.load_gamma(p, k_lo + (tid + (int64_t)rl * CONSUMERS) * 8);  // a model parameter: may be read early
     pdl_wait();  // activations may be written by the previous kernel in the stream
 
     // ---- phase 1: prologue statistics of this CTA's K range, per row
@@ -548,10 +554,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       float amax[MT], ssq[MT];
   #pragma unroll
       for (int m = 0; m < MT; m++) amax[m] = ssq[m] = 0.f;
-      for (int r = 0; r < rounds; r++) {
+      auto stat_round = [&](int r, bool gam) {
         const int64_t i8 = (int64_t)r * CONSUMERS + tid;
         if (i8 < n8) {
-          if (r > 0) act.load_gamma(p, k_lo + i8 * 8);
+          if (gam) act.load_gamma(p, k_lo + i8 * 8);
           act.load(p, M, k_lo + i8 * 8);
   #pragma unroll
           for (int m = 0; m < MT; m++) {
@@ -563,6 +569,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
             }
           }
         }
+      };
+      if constexpr (REV) {
+        for (int r = rl; r >= 0; r--) stat_round(r, r < rl);
+      } else {
+        for (int r = 0; r < rounds; r++) stat_round(r, r > 0);
       }
   #pragma unroll
       for (int m = 0; m < MT; m++) {
@@ -627,7 +638,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       for (int r = 0; r < rounds2; r++) {
         const int64_t i8 = (int64_t)r * CONSUMERS + tid;
         const bool inb = i8 < n8f, valid = i8 < n8;
-        if (valid && rounds > 1) {
+        if (valid && (REV ? r > 0 : rounds > 1)) {  // (REV: round 0 is still in the slice)
           act.load_gamma(p, k_lo + i8 * 8);
           act.load(p, M, k_lo + i8 * 8);
         }
