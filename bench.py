@@ -149,8 +149,9 @@ def max_over_ranks(v: float, ws: int, device) -> float:
 # kernel reports no traffic until it is captured again.
 KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
 TRAFFIC = {
-    "82a3d2f54ef8ae1f": {"bytes_per_launch": 98126080,
-                         "source": "profiles/forward_gate_up_w4a8_k5120.md (ncu --set full, one gate/up launch)"},
+    "0f3f5b1ea3945020": {"bytes_per_launch": 97141248,
+                         "source": "profiles/forward_gate_up_w4a8_k5120.md (ncu dram__bytes_read.sum + "
+                                   "dram__bytes_write.sum, one gate/up launch)"},
 }
 
 
