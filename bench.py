@@ -7,10 +7,16 @@ down, none before o; codes uniform, scales ~ U(0.005, 0.02), activations
 ~ N(0,1) bf16, gamma ~ U(0.5, 1.5).  11,586,764,800 bytes of packed weights,
 all distinct, so every step streams them from HBM (inputs larger than L2).
 
-One step = the 448 qlin_forward calls of the stack at one M, replayed as one
-CUDA graph (each call is one cluster launch of the fused prologue + GEMV
-kernel, with programmatic dependent launch).  value = weight bytes per step / step time at
-M = 1; the same at M = 8 and t(M=8)/t(M=1) are reported alongside.
+One step = the 256 launches of the stack at one M (per layer: q/k/v and
+gate/up as multi-weight launches on their shared input, o and down alone),
+replayed as one CUDA graph (each call is one cluster launch of the fused
+prologue + GEMV kernel, with programmatic dependent launch).  value = weight
+bytes per step / step time at M = 1; the same at M = 8 and t(M=8)/t(M=1) are
+reported alongside (last on the line), and the 448-launch step with every
+linear alone.  e2e replays the graph with the step's activations copied in
+from pinned host memory and its outputs copied back; e2e_eager does the same
+with the launches enqueued call by call (no graph) and reports the host time
+per call.
 
 --impl reference times the CPU oracle (the method's plain definition) on a
 bounded sample of the same workload: one layer at M = 1.
@@ -149,10 +155,9 @@ def max_over_ranks(v: float, ws: int, device) -> float:
 # kernel reports no traffic until it is captured again.
 KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
 TRAFFIC = {
-    "0f3f5b1ea3945020": {"bytes_per_launch": 97141248,
-                         "source": "profiles/forward_gate_up_w4a8_k5120.md (ncu dram__bytes_read.sum + "
-                                   "dram__bytes_write.sum, one gate/up launch)"},
+    "0f3f5b1ea3945020": {"bytes_per_launch": 97141248},
 }
+TRAFFIC_METRICS = "ncu dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch"
 
 
 def kernel_hash() -> str:
@@ -710,6 +715,37 @@ def main():
     te2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     gbs_e2e = job_gbs(world, wb, te2e)
 
+    # the same end to end without a graph: each step's launches enqueued call
+    # by call through the binding (the C ABI underneath), as an application
+    # that does not capture graphs runs them
+    grps1 = stack.groups(1)
+
+    def eager_step():
+        d_act.copy_(h_act, non_blocking=True)
+        n = 0
+        for grp in grps1:
+            n += stack.launch(grp, stream, True)
+        h_out.copy_(d_out, non_blocking=True)
+        return n
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            eager_step()
+        torch.cuda.synchronize()
+        host_us = []  # host time to enqueue one step, from an idle queue
+        for _ in range(5):
+            t0 = time.perf_counter()
+            n_eager = eager_step()
+            host_us.append((time.perf_counter() - t0) * 1e6 / n_eager)
+            torch.cuda.synchronize()
+        barrier(world)
+        e0.record(stream)
+        for _ in range(args.steps):
+            eager_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    te2e_eager = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+
     assert qlin.read_device_status(stack.ws) == qlin.OK
 
     cpu = None
@@ -740,8 +776,6 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": 100.0 * gbs1 / world / peak, "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
         "pct_of_8tbs_spec": 100.0 * gbs1 / world / 8000.0,
-        "m8": {"value": gbs8, "ms_per_step": t8, "pct_of_hbm_peak": 100.0 * gbs8 / world / peak},
-        "t8_over_t1": t8 / t1,
         "separate_launches": {"launches_per_step": ncalls_sep, "value": job_gbs(world, wb, ts1),
                               "ms_per_step": ts1, "m8": job_gbs(world, wb, ts8), "t8_over_t1": ts8 / ts1},
         "per_group": per,
@@ -752,12 +786,19 @@ def main():
                      "kernel": "qlin_forward_kernel<4,128,0> (RMSNorm prologue): the gate/up multi-weight launch, M=1, "
                                f"{gu_bytes} algorithmic bytes per launch, {gu_us:.2f} us per launch (CUDA events, "
                                "64 launches in a graph)",
-                     "traffic_source": traffic["source"] if traffic else "kernel changed since the last ncu capture"},
+                     "traffic_source": (f"{TRAFFIC_METRICS}, kernel sources {kernel_hash()}" if traffic
+                                        else f"kernel sources {kernel_hash()} changed since the last ncu capture")},
         "cpu_baseline": cpu,
         "e2e": {"value": gbs_e2e, "unit": "GB/s", "ms_per_step": te2e,
                 "h2d_bytes_per_step": h_act.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 4},
+        "e2e_eager": {"value": job_gbs(world, wb, te2e_eager), "unit": "GB/s", "ms_per_step": te2e_eager,
+                      "launches_per_step": n_eager, "host_us_per_call": statistics.median(host_us),
+                      "h2d_bytes_per_step": h_act.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 4},
         "gpu_launches": ncalls * args.steps,
         "clocks": clocks,
+        # the second half of the headline, last on the line
+        "m8": {"value": gbs8, "ms_per_step": t8, "pct_of_hbm_peak": 100.0 * gbs8 / world / peak},
+        "t8_over_t1": t8 / t1,
     }
     if rank == 0:
         print(json.dumps(line))

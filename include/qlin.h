@@ -177,7 +177,9 @@ qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * method's tolerance allows); group sums are exact integers; y is accumulated
  * in fp32 in a fixed order that depends on (N, K, G) and the device, never on
  * M or on the other rows, so row m of an 8-row call equals the same row run
- * alone.  One kernel is enqueued: a cluster of CTAs per 256 output rows
+ * alone: the split of K over the CTAs of a cluster is planned for 8 rows
+ * whatever M is, and M changes only how deep the weight ring is.  One kernel
+ * is enqueued: a cluster of CTAs per 256 output rows
  * splits K, computes the prologue and the row statistics in shared memory,
  * streams the weights through the tensor cores and reduces its split-K
  * partial sums through distributed shared memory.
@@ -235,6 +237,9 @@ qlin_status qlin_forward(int fmt, int prologue, int M, int64_t N, int64_t K, int
  *   Other arguments, numerics and errors as qlin_forward.  One launch is
  *   sized for min(E, M * topk) experts; the experts actually routed take its
  *   row blocks in increasing id order, the remaining blocks return at once.
+ *   The split of K is planned for min(E, 8 * topk) experts, so for a given
+ *   bank (E, N, K, G) and topk, token m's output does not depend on M or on
+ *   the other tokens' routing.
  *   Under QLIN_FLAG_PDL the weights are not streamed before the previous
  *   kernel completes (the routing decides which weights).
  */
@@ -273,7 +278,8 @@ qlin_status qlin_forward_multi(int fmt, int prologue, int M, int n, const int64_
                                size_t ws_bytes, unsigned flags, void* stream);
 
 /* Launch shape of qlin_forward's GEMV on the current device: CTAs, stream
- * units (128 rows x KB columns) and bytes of `packed` read per call. */
+ * units (128 rows x KB columns) and bytes of `packed` read per call.  The
+ * CTAs are the same for every M (the split of K does not depend on M). */
 qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G,
                                      int64_t* ctas, int64_t* units, int64_t* stream_bytes);
 

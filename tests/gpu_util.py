@@ -66,3 +66,26 @@ def sample_cols(N: int, n: int = 384, seed: int = 0) -> np.ndarray:
     edge = np.r_[np.arange(min(N, 16)), np.arange(max(0, N - 16), N)]
     pick = rng.choice(N, size=min(N, n), replace=False)
     return np.unique(np.r_[edge, pick])
+
+
+def multi_cases(fmt, kind, M, Ns, K, G, seed, scale_range=(0.005, 0.02)):
+    """One case per weight of a multi-weight launch; every weight reads the
+    first case's activation (and gamma).  A zero N gives None."""
+    base = inputs.make_case(fmt, kind, M, max(Ns[0], 16), K, G, seed=seed, scale_range=scale_range)
+    out = []
+    for l, N in enumerate(Ns):
+        if N == 0:
+            out.append(None)
+            continue
+        c = inputs.make_case(fmt, kind, M, N, K, G, seed=seed + 101 * (l + 1), scale_range=scale_range)
+        for k in ("x", "gate", "up", "gamma"):
+            setattr(c, k, getattr(base, k))
+        out.append(c)
+    return base, out
+
+
+def acts(c, d, M=None):
+    """The activation arguments of a call, optionally only the first M rows."""
+    sl = slice(None) if M is None else slice(0, M)
+    take = (lambda t: t[sl].contiguous() if t is not None else None)
+    return dict(x=take(d["x"]), gate=take(d["gate"]), up=take(d["up"]), gamma=d["gamma"], eps=c.eps)

@@ -15,7 +15,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import DEV, assert_y_close, boundary_ok, built, device_case, oracle_forward, sample_cols
+from gpu_util import (DEV, assert_y_close, boundary_ok, built, device_case, multi_cases, oracle_forward,
+                      sample_cols)
 from oracle import qlin_oracle as O
 from w6a8_quantized_linear_gb300 import inputs, qlin
 
@@ -54,7 +55,8 @@ CASES = [("c1_w4a8_small", 1), ("c2_w4a8_rmsnorm", 1), ("c2_w4a8_rmsnorm", 2), (
 
 @pytest.mark.parametrize("name,M", CASES)
 def test_config_full_size_sampled(name, M):
-    c = inputs.config_case(name, M, seed=M)
+    # the first configuration states its seed (0); the others name none
+    c = inputs.config_case(name, M, seed=0 if name == "c1_w4a8_small" else M)
     d = device_case(c)
     ws = qlin.new_workspace(qlin.forward_workspace_bytes(c.fmt, c.N, c.K, c.G))
     y = qlin.forward(c.fmt, c.kind, d["w"], c.N, c.K, c.G, ws=ws, flags=qlin.FLAG_PDL, **_acts(c, d))
@@ -69,18 +71,7 @@ def test_config_full_size_sampled(name, M):
 
 # ------------------------------------------------------------------ multi-weight
 def _multi_cases(fmt, kind, M, Ns, K, G, seed):
-    """One case per weight; every weight reads the first case's activation."""
-    base = inputs.make_case(fmt, kind, M, max(Ns[0], 16), K, G, seed=seed)
-    out = []
-    for l, N in enumerate(Ns):
-        if N == 0:
-            out.append(None)
-            continue
-        c = inputs.make_case(fmt, kind, M, N, K, G, seed=seed + 101 * (l + 1))
-        for k in ("x", "gate", "up", "gamma"):
-            setattr(c, k, getattr(base, k))
-        out.append(c)
-    return base, out
+    return multi_cases(fmt, kind, M, Ns, K, G, seed)
 
 
 MULTI = [("w4a8", "rmsnorm", 3, (272, 48, 48), 384, 128),

@@ -42,16 +42,14 @@ def test_noalloc_matches_forward_two_calls_in_a_row():
     assert_y_close(again.cpu().numpy(), refs[0].double().cpu().numpy(), "noalloc repeat")
 
 
-def test_noalloc_rejects_shapes_beyond_its_array():
-    cands = [("w4a8", 16, 65536, 32), ("w6a8", 16, 65536, 256), ("w4a8", 17408, 5120, 128)]
-    big = [(f, N, K, G) for f, N, K, G in cands
-           if qlin.check_shape(f, N, K, G) == qlin.OK and qlin.forward_workspace_bytes(f, N, K, G) > LIMIT]
-    if not big:
-        pytest.skip("every supported shape's workspace fits the library's array")
-    f, N, K, G = big[0]
-    w = torch.zeros(qlin.packed_bytes(f, N, K, G), dtype=torch.uint8, device=DEV)
-    x = torch.zeros(1, K, dtype=torch.bfloat16, device=DEV)
-    y = torch.empty(1, N, dtype=torch.float32, device=DEV)
-    st = qlin.lib().qlin_forward_noalloc(qlin.FORMATS[f], 0, 1, N, K, G, w.data_ptr(), x.data_ptr(), None, None,
-                                         None, 1e-6, y.data_ptr(), 0, torch.cuda.current_stream().cuda_stream)
-    assert st == qlin.ERR_WORKSPACE
+def test_noalloc_array_holds_every_supported_workspace():
+    """The library's array must hold the workspace of every shape the backend
+    supports (the largest K, the narrowest and widest groups, both formats),
+    so that no supported call is refused for size.  If the forward workspace
+    ever grows, this fails before a caller meets QLIN_ERR_WORKSPACE."""
+    shapes = [("w4a8", 16, 65536, 4), ("w4a8", 16, 65536, 32), ("w4a8", 1 << 20, 65536, 256),
+              ("w6a8", 16, 65536, 16), ("w6a8", 1 << 20, 65536, 256), ("w4a8", 17408, 5120, 128),
+              ("w6a8", 5120, 17408, 32)]
+    for f, N, K, G in shapes:
+        assert qlin.check_shape(f, N, K, G) == qlin.OK, (f, N, K, G)
+        assert qlin.forward_workspace_bytes(f, N, K, G) <= LIMIT, (f, N, K, G)

@@ -30,10 +30,34 @@ constexpr int64_t SMEM_TWO_PER_SM = 110 * 1024;  // dynamic bytes that leave roo
 constexpr int64_t SMEM_MAX = 220 * 1024;         // dynamic bytes of a CTA alone on its SM (static shared
                                                  // memory and the per-CTA reservation share the 227 KB)
 
+// How a forward call is laid out on the device.
+struct Plan {
+  int C = 1;          // CTAs per cluster: the split of K for one 256-row block
+  int64_t NB = 0;     // 256-row blocks (clusters)
+  int upc = 0;        // stream units per CTA, at most
+  int stages = 0;
+  bool alone = false; // carved for one CTA per SM (the whole shared-memory budget)
+  int64_t stage_bytes = 0, b_off = 0, red_off = 0, smem = 0;
+};
+
+// What a launch's cluster size depends on: the kernel, the K geometry and
+// the launch's row blocks -- never the rows M of the activation.
+struct PlanKey {
+  const void* fn;
+  int64_t K, G, NB;
+  bool operator<(const PlanKey& o) const {
+    if (fn != o.fn) return fn < o.fn;
+    if (K != o.K) return K < o.K;
+    if (G != o.G) return G < o.G;
+    return NB < o.NB;
+  }
+};
+
 struct DevCache {
   bool init = false;
   int sms = 0;
   std::map<std::pair<std::pair<const void*, int>, int64_t>, int> clusters;  // (kernel, C, smem) -> max active clusters
+  std::map<PlanKey, Plan> plans;  // the plan at MAX_M rows, per launch geometry
 };
 
 std::mutex g_mu;
@@ -120,15 +144,6 @@ qlin_status device_cache(DevCache** out) {
   return QLIN_OK;
 }
 
-// How a forward call is laid out on the device.
-struct Plan {
-  int C = 1;          // CTAs per cluster: the split of K for one 256-row block
-  int64_t NB = 0;     // 256-row blocks (clusters)
-  int upc = 0;        // stream units per CTA, at most
-  int stages = 0;
-  int64_t stage_bytes = 0, b_off = 0, red_off = 0, smem = 0;
-};
-
 // Shared-memory carve: [extra][stages][activation operand][split-K slots]
 // (extra: the codebook table, which the kernel expects at offset 0).  Fails
 // when the budget holds fewer than min_stages stages (or the CTA's units).
@@ -179,13 +194,27 @@ int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
 // shared-memory activation operand allows, the carve and the number of
 // clusters the device holds at once give the waves of the launch; the cost is
 // waves x stream units of the busiest CTA.  The cheapest C wins, ties going
-// to the smaller cluster.  Caller holds g_mu.
-qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int mode, Plan* out) {
+// to the smaller cluster.  The search carves the operand for MAX_M rows, so C
+// -- and with it the split-K ranges, the rank order of the fp32 partial sums
+// and of the RMSNorm statistics -- is the same for every M; plan_for_rows
+// then re-carves only the ring stages for the launch's rows.  Plans are
+// cached per launch geometry.  Caller holds g_mu.
+qlin_status make_plan(const Geo& g, int64_t NB, DevCache& dc, int mode, Plan* out) {
+  // the test-hook mode computes exactly what the plain mode does, so it is
+  // planned as the plain kernel (same C, same order of the sums)
+  const void* fn = forward_fn(g.bits, g.G, mode == 3 ? 0 : mode);
+  const PlanKey key{fn, g.K, g.G, NB};
+  auto it = dc.plans.find(key);
+  if (it != dc.plans.end()) {
+    *out = it->second;
+    return QLIN_OK;
+  }
+  const int64_t bbf = bblock_bytes(g.KB, g.G, MAX_M);
   const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
   const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
   const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
   if (cmin > cmax) return QLIN_ERR_UNSUPPORTED;
-  const void* fn = forward_fn(g.bits, g.G, mode);
+  const int64_t extra = mode == 2 ? CODEBOOK_LUT_BYTES : 0;
   bool found = false;
   int64_t best_cost = 0;
   for (int64_t c = cmin; c <= cmax; c++) {
@@ -193,10 +222,10 @@ qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int m
     pl.NB = NB;
     pl.C = (int)c;
     pl.upc = (int)((g.J + c - 1) / c);
-    const int64_t extra = mode == 2 ? CODEBOOK_LUT_BYTES : 0;
     // two CTAs per SM need at least two stages each (four units in flight per
     // SM keep DRAM busy); with fewer, one CTA per SM gets the whole budget
-    if (!(carve(g, bbf, pl, SMEM_TWO_PER_SM, 2, extra) || carve(g, bbf, pl, SMEM_MAX, 2, extra))) continue;
+    pl.alone = !carve(g, bbf, pl, SMEM_TWO_PER_SM, 2, extra);
+    if (pl.alone && !carve(g, bbf, pl, SMEM_MAX, 2, extra)) continue;
     const int n = active_clusters(dc, fn, pl.C, pl.smem);
     if (n < 1) continue;
     const int64_t cost = (NB + n - 1) / n * pl.upc;
@@ -206,7 +235,22 @@ qlin_status make_plan(const Geo& g, int64_t NB, int64_t bbf, DevCache& dc, int m
       *out = pl;
     }
   }
-  return found ? QLIN_OK : QLIN_ERR_UNSUPPORTED;
+  if (!found) return QLIN_ERR_UNSUPPORTED;
+  dc.plans[key] = *out;
+  return QLIN_OK;
+}
+
+// The plan for a launch of M rows: the cluster size of the MAX_M plan, with
+// the ring re-carved in the same budget for the (smaller or equal) operand
+// of M rows.  Stages change no summation order.
+Plan plan_for_rows(const Geo& g, const Plan& at_max, int M, int mode) {
+  Plan pl = at_max;
+  if (M < MAX_M) {
+    const int64_t extra = mode == 2 ? CODEBOOK_LUT_BYTES : 0;
+    Plan r = at_max;
+    if (carve(g, bblock_bytes(g.KB, g.G, M), r, at_max.alone ? SMEM_MAX : SMEM_TWO_PER_SM, 2, extra)) pl = r;
+  }
+  return pl;
 }
 
 qlin_status launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args, int cluster_x,
@@ -272,12 +316,12 @@ struct Outputs {  // test exports of a single-weight call
   float* s = nullptr;
 };
 
-// One launch over n weights that share the format, K, G and the activation
-// input: argument checks, the plan, the parameter block, the launch.
 // The plan, the shared part of the parameter block and the launch.  p holds
-// the weights (table or expert bank) already; NB is the launch's row blocks.
+// the weights (table or expert bank) already; NB is the launch's row blocks,
+// NB_plan the row blocks its cluster size is chosen for (the same for every
+// M: NB itself for a weight table, the most experts an expert bank can route).
 qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, int64_t G, int64_t NB,
-                            const void* x, const void* gate, const void* up, const float* gamma, float eps,
+                            int64_t NB_plan, const void* x, const void* gate, const void* up, const float* gamma, float eps,
                             const Outputs& out, void* ws, unsigned flags, void* stream, int64_t fault_unit) {
   const Geo g = make_geo(fmt, 0, K, G);  // the K geometry every weight shares
   const bool test_hooks = out.acc || out.q || out.s || fault_unit >= 0;
@@ -288,9 +332,11 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
     DevCache* dc = nullptr;
     qlin_status st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, NB, bblock_bytes(g.KB, G, M), *dc, mode, &pl);
+    st = make_plan(g, NB_plan, *dc, mode, &pl);
     if (st != QLIN_OK) return st;
   }
+  pl = plan_for_rows(g, pl, M, mode);
+  pl.NB = NB;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.gate = static_cast<const __nv_bfloat16*>(gate);
   p.up = static_cast<const __nv_bfloat16*>(up);
@@ -365,7 +411,8 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
   }
   p.n_lin = nl;
   p.codebook = codebook;
-  return plan_and_launch(p, fmt, kind, M, K, G, NB, x, gate, up, gamma, eps, out, ws, flags, stream, fault_unit);
+  return plan_and_launch(p, fmt, kind, M, K, G, NB, NB, x, gate, up, gamma, eps, out, ws, flags, stream,
+                         fault_unit);
 }
 
 // An expert bank: argument checks, then the routed-expert launch.
@@ -397,9 +444,13 @@ qlin_status moe_impl(int fmt, int kind, int M, int E, int64_t N, int64_t K, int6
   p.bank = static_cast<const uint8_t*>(bank);
   p.bank_bias = bias;
   p.ymoe = y;
-  const int64_t slots = std::min<int64_t>(E, (int64_t)M * topk);  // routed experts, at most
-  return plan_and_launch(p, fmt, kind, M, K, G, slots * p.nbe, x, gate, up, gamma, eps, Outputs(), ws, flags,
-                         stream, -1);
+  // routed experts, at most: for this launch, and for any launch of MAX_M
+  // tokens (which fixes the cluster size, so a token's output does not
+  // depend on how many other tokens share the launch)
+  const int64_t slots = std::min<int64_t>(E, (int64_t)M * topk);
+  const int64_t slots_plan = std::min<int64_t>(E, (int64_t)MAX_M * topk);
+  return plan_and_launch(p, fmt, kind, M, K, G, slots * p.nbe, slots_plan * p.nbe, x, gate, up, gamma, eps,
+                         Outputs(), ws, flags, stream, -1);
 }
 
 // ---------------------------------------------------------------------------
@@ -603,7 +654,7 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, i
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, row_blocks(N), bblock_bytes(g.KB, G, MAX_M), *dc, 0, &pl);
+    st = make_plan(g, row_blocks(N), *dc, 0, &pl);
     if (st != QLIN_OK) return st;
   }
   *ctas = (int64_t)pl.C * pl.NB;
