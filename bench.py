@@ -285,7 +285,8 @@ class Stack:
 def next_rows(stack, stream, iters: int, peak: float):
     """The widened paths on the stack's gate weights (17408 x 5120, G = 128,
     RMSNorm prologue), 64 launches on 64 distinct weights in one graph each:
-    the single-weight launch; 8 weights of the same shape in the codebook
+    the single-weight launch; the same launch on the tcgen05 main loop (8
+    weights in its row layout, eight passes); 8 weights of the same shape in the codebook
     stream layout with a 16-level codebook (378 MB, more than L2, eight
     passes); and each stack weight read as an expert bank of 17 experts x
     1024 rows (8 routed experts for one token; 2 per token for 8 tokens)."""
@@ -328,6 +329,22 @@ def next_rows(stack, stream, iters: int, peak: float):
         qlin.forward_codebook("w4a8", "rmsnorm", w, cb, N, K, G, x=x1, gamma=gamma, y=y[:N].view(1, N),
                               ws=stack.ws, flags=qlin.FLAG_PDL, stream=stream)
 
+    # the tcgen05 main loop (test export) on the same gate shape: 8 distinct
+    # weights in its row layout (378 MB, more than L2), eight passes
+    tc_weights = []
+    rws = torch.empty(qlin.repack_workspace_bytes("w4a8", N, K, G)[1], dtype=torch.uint8, device=stack.dev)
+    for _ in range(8):
+        w = torch.empty(wbytes, dtype=torch.uint8, device=stack.dev)
+        w[:ncb] = torch.randint(0, 256, (ncb,), generator=gw, dtype=torch.uint8, device=stack.dev)
+        w[ncb:].view(torch.float32).uniform_(lo, hi, generator=gw)
+        qlin.debug_repack_tcgen05(w, "w4a8", N, K, G, ws=rws)
+        tc_weights.append(w)
+    del rws
+
+    def tcgen05(w):
+        qlin.debug_forward_tcgen05("w4a8", "rmsnorm", w, N, K, G, x=x1, gamma=gamma, y=y[:N].view(1, N),
+                                   ws=stack.ws, flags=qlin.FLAG_PDL, stream=stream)
+
     def moe(ids, x):
         def f(w):
             qlin.forward_moe("w4a8", "rmsnorm", w, E, NE, K, G, ids, x=x, gamma=gamma,
@@ -335,7 +352,8 @@ def next_rows(stack, stream, iters: int, peak: float):
                              flags=qlin.FLAG_PDL, stream=stream)
         return f
 
-    cases = [("single_weight", plain, wbytes), ("codebook", codebook, wbytes, cb_weights),
+    cases = [("single_weight", plain, wbytes), ("tcgen05_single_weight", tcgen05, wbytes, tc_weights),
+             ("codebook", codebook, wbytes, cb_weights),
              ("moe_m1_top8", moe(ids1, x1), wbytes * 8 // E), ("moe_m8_top2", moe(ids8, x8),
                                                                 wbytes * len(set(ids8.flatten().tolist())) // E)]
     out = {}
@@ -356,7 +374,7 @@ def next_rows(stack, stream, iters: int, peak: float):
         out[name] = {"us_per_launch": us, "weight_bytes_per_launch": nbytes, "GB/s": nbytes / (us * 1e-6) / 1e9,
                      "frac_of_measured_hbm": nbytes / (us * 1e-6) / 1e9 / peak}
         del g
-    del cb_weights
+    del cb_weights, tc_weights
     return out
 
 

@@ -315,6 +315,42 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
                                      int64_t unit, void* stream);
 
 /*
+ * Test exports of the second main loop, on the 5th-generation tensor cores
+ * (tcgen05.mma with the fp16 weight operand in tensor memory, accumulators in
+ * tensor memory), kept to measure it against qlin_forward's warp-level MMA
+ * loop; it computes the same results ("Doubling the LLM token rate in
+ * ComfyUI", section "Optimising the linear kernel": the M <= 8 activation
+ * rows on the narrow side of the tensor-core product).  It is slower on this
+ * path: every 4-bit code is unpacked on the CUDA cores either way, and the
+ * tensor-memory stores, the hand-offs between warps and the MMA issue (one
+ * 128 x 16 step per instruction) cost more than the warp-level MMAs they
+ * replace.
+ *
+ * qlin_debug_repack_tcgen05: qlin_repack into the row layout this loop reads
+ *   (G >= 32): per unit of R rows and W columns,
+ *     scale block  R*(W/G) fp32, [group][row];
+ *     4-bit plane  for each 32-wide k chunk c, for each row: 4 words, word j
+ *                  holding the low 4 bits of the codes of k = 32c + 8j + i at
+ *                  bits 4i (i = 0..7);
+ *     6-bit codes only, then the 2-bit plane: for each chunk, for each row: 2
+ *                  words; word h holds the top 2 bits of the codes of words
+ *                  2h (at offset 0) and 2h+1 (at offset 2), code i of a word
+ *                  at bit P(i) + offset, P = (4, 8, 0, 12, 20, 24, 16, 28).
+ *   Arguments and errors as qlin_repack; QLIN_ERR_UNSUPPORTED for G < 32.
+ * qlin_debug_forward_tcgen05: qlin_debug_forward on a weight repacked by
+ *   qlin_debug_repack_tcgen05 (y required; acc, q, s may be NULL), with
+ *   qlin_forward's flags.  Its split of K is planned for its own shared-memory
+ *   operand, so y may differ from qlin_forward's in the last bits (the order
+ *   of the fp32 partial sums); the group sums are the same exact integers.
+ */
+qlin_status qlin_debug_repack_tcgen05(int fmt, int64_t N, int64_t K, int64_t G, void* buf, void* ws,
+                                      size_t ws_bytes, void* stream);
+qlin_status qlin_debug_forward_tcgen05(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
+                                       const void* packed, const void* x, const void* gate, const void* up,
+                                       const float* gamma, float eps, float* y, int32_t* acc, int8_t* q, float* s,
+                                       void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/*
  * qlin_forward without a caller workspace.  The method has no counterpart: this
  * is for callers that cannot allocate device memory where they run the layer
  * (a host whose memory pool owns the whole device and forbids cudaMalloc, code

@@ -372,7 +372,18 @@ def unpack_stream(fmt: str, N: int, K: int, G: int, buf, layout: str = "plain") 
     ``layout="codebook"`` (4-bit codes whose levels come from a codebook) is
     the same stream except inside a plane word: A-register i's two elements
     sit in byte i, the even k at bits 8i..8i+3 and the odd k at 8i+4..8i+7.
+
+    ``layout="rows"`` (the row layout of the second main loop) keeps the
+    tiles and units but orders each unit by rows: the scale block is
+    [group][row]; the 4-bit plane holds, for each 32-wide k chunk c and each
+    row, 4 little-endian words, word j holding the low 4 bits of the codes of
+    k = 32c + 8j + i at bits 4i; for 6-bit codes the 2-bit plane follows,
+    for each chunk and row 2 words, word h holding the top 2 bits of the codes
+    of words 2h and 2h+1 of that row and chunk, code i at bit TOP2_POS[i]
+    (plus 2 for word 2h+1).
     """
+    if layout == "rows":
+        return _unpack_stream_rows(fmt, N, K, G, buf)
     assert layout in ("plain", "codebook")
     assert layout == "plain" or fmt == "w4a8", "only 4-bit codes have the codebook layout"
     b = BITS[fmt]
@@ -412,6 +423,44 @@ def unpack_stream(fmt: str, N: int, K: int, G: int, buf, layout: str = "plain") 
             tile = np.empty((S, 16, P, 32), dtype=np.int64)
             tile[:, ROW, :, KIP] = val.transpose(2, 3, 4, 5, 0, 1).astype(np.int64)
             codes[t0:t0 + R, k0:k0 + W] = tile.reshape(R, W)
+    assert pos == file_bytes(fmt, N, K, G), (pos, file_bytes(fmt, N, K, G))
+    assert codes.min() >= 0, "stream does not cover every (n, k)"
+    return codes, sw
+
+
+# Bit of the top 2 bits of code i (of a 4-bit plane word) in the row layout's
+# 2-bit plane word, for the first word of the pair (the second is 2 bits up).
+TOP2_POS = (4, 8, 0, 12, 20, 24, 16, 28)
+
+
+def _unpack_stream_rows(fmt: str, N: int, K: int, G: int, buf) -> tuple[np.ndarray, np.ndarray]:
+    """The row layout (see ``unpack_stream``), read unit by unit."""
+    b = BITS[fmt]
+    buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
+    assert N % 16 == 0 and K % 32 == 0 and K % G == 0 and G >= 32
+    KB = stream_kb(G)
+    i = np.arange(8)
+    j = np.arange(4)
+    top_shift = (np.array(TOP2_POS)[None, :] + 2 * (j[:, None] % 2)).astype(np.uint32)   # [word j, code i]
+    codes = np.full((N, K), -1, dtype=np.int64)
+    sw = np.full((N, K // G), np.nan, dtype=np.float32)
+    pos = 0
+    for t0 in range(0, N, STREAM_TN):
+        R = min(STREAM_TN, N - t0)
+        for k0 in range(0, K, KB):
+            W = min(KB, K - k0)
+            ng, C = W // G, W // 32
+            f = np.frombuffer(buf[pos:pos + 4 * R * ng].tobytes(), dtype="<f4").reshape(ng, R)
+            pos += 4 * R * ng
+            sw[t0:t0 + R, k0 // G:k0 // G + ng] = f.T
+            words = np.frombuffer(buf[pos:pos + R * W // 2].tobytes(), dtype="<u4").reshape(C, R, 4)
+            pos += R * W // 2
+            val = (words[..., None] >> (4 * i).astype(np.uint32)) & 0xF                 # [chunk, row, word, code]
+            if b == 6:
+                top = np.frombuffer(buf[pos:pos + R * W // 4].tobytes(), dtype="<u4").reshape(C, R, 2)
+                pos += R * W // 4
+                val = val | (((top[:, :, j // 2][..., None] >> top_shift) & 0x3) << 4)
+            codes[t0:t0 + R, k0:k0 + W] = val.transpose(1, 0, 2, 3).reshape(R, W).astype(np.int64)
     assert pos == file_bytes(fmt, N, K, G), (pos, file_bytes(fmt, N, K, G))
     assert codes.min() >= 0, "stream does not cover every (n, k)"
     return codes, sw

@@ -330,6 +330,69 @@ def check_stream_positions_codebook(O):
         assert np.unique(key).size == N * K
 
 
+def check_stream_positions_rows(O):
+    """The row layout: single codes at hand-derived positions (both formats),
+    the scale order, and every code read from its own field (bijection) on a
+    ragged tile, several units and G > 128."""
+    g = read_golden("stream_positions_rows.txt")
+    N, K, G = 16, 32, 32
+    rows = [[int(key)] + [int(v) for v in rest] for key in ("0", "9", "3", "15", "5") for rest in g[key]]
+    for fmt in ("w4a8", "w6a8"):
+        size = O.file_bytes(fmt, N, K, G)
+        for n, k, nb, ns, hb, hs in rows:
+            buf = np.zeros(size, dtype=np.uint8)
+            buf[nb] = 0x5 << ns
+            if fmt == "w6a8":
+                buf[hb] = 0x2 << hs
+            codes, _ = O.unpack_stream(fmt, N, K, G, buf, layout="rows")
+            want = np.zeros((N, K), dtype=np.int64)
+            want[n, k] = 5 + (32 if fmt == "w6a8" else 0)
+            assert np.array_equal(codes, want), (fmt, n, k, np.argwhere(codes))
+        buf = np.zeros(size, dtype=np.uint8)
+        buf[:64] = np.arange(16, dtype="<f4").view(np.uint8)
+        _, sw = O.unpack_stream(fmt, N, K, G, buf, layout="rows")
+        for slot, row in enumerate(int(v) for v in g["scale_rows"][0]):
+            assert sw[row, 0] == slot, (fmt, row, sw[:, 0])
+        # two chunks and two groups in one unit: chunk-major planes, [group][row] scales
+        n, k, nb, ns, hb, hs = (int(v) for v in g["wide"][0])
+        size = O.file_bytes(fmt, 16, 64, 32)
+        buf = np.zeros(size, dtype=np.uint8)
+        buf[nb] = 0x5 << ns
+        if fmt == "w6a8":
+            buf[hb] = 0x2 << hs
+        codes, _ = O.unpack_stream(fmt, 16, 64, 32, buf, layout="rows")
+        want = np.zeros((16, 64), dtype=np.int64)
+        want[n, k] = 5 + (32 if fmt == "w6a8" else 0)
+        assert np.array_equal(codes, want), (fmt, n, k, np.argwhere(codes))
+        row, grp, byte = (int(v) for v in g["wide_scale"][0])
+        buf = np.zeros(size, dtype=np.uint8)
+        buf[byte:byte + 4] = np.array([7.0], dtype="<f4").view(np.uint8)
+        _, sw = O.unpack_stream(fmt, 16, 64, 32, buf, layout="rows")
+        assert sw[row, grp] == 7.0 and np.count_nonzero(sw) == 1, (fmt, np.argwhere(sw))
+    for fmt, N, K, G in (("w4a8", 144, 160, 32), ("w6a8", 144, 160, 32), ("w4a8", 32, 512, 256), ("w6a8", 16, 384, 64)):
+        size = O.file_bytes(fmt, N, K, G)
+        assert size < (1 << 16)
+        p = np.arange(size)
+        src = np.zeros((N, K), dtype=np.int64)
+        for j in range(4):
+            d = ((p >> (4 * j)) & 0xF).astype(np.uint8)
+            codes, _ = O.unpack_stream(fmt, N, K, G, d | (d << 4), layout="rows")
+            src |= (codes & 0xF) << (4 * j)
+        half, _ = O.unpack_stream(fmt, N, K, G, np.full(size, 0x10, dtype=np.uint8), layout="rows")
+        key = src * 2 + (half & 0xF)
+        assert np.unique(key).size == N * K, fmt
+        if fmt == "w6a8":
+            hsrc = np.zeros((N, K), dtype=np.int64)
+            for j in range(8):
+                d = ((p >> (2 * j)) & 0x3).astype(np.uint8)
+                codes, _ = O.unpack_stream(fmt, N, K, G, d * np.uint8(0x55), layout="rows")
+                hsrc |= (codes >> 4) << (2 * j)
+            slot, _ = O.unpack_stream(fmt, N, K, G, np.full(size, 0b11100100, dtype=np.uint8), layout="rows")
+            hkey = hsrc * 4 + (slot >> 4)
+            assert np.unique(hkey).size == N * K, fmt
+            assert not np.intersect1d(src, hsrc).size, "2-bit plane shares bytes with the 4-bit plane"
+
+
 def check_bias(O, seed=9):
     """A float bias is added once, unscaled, to every row: with every level zero
     y equals the bias exactly; sampled columns take the matching entries."""

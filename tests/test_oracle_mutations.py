@@ -37,12 +37,16 @@ MUTANTS = {
     "codebook_index_flipped": ("astype(np.float64)[np.asarray(codes)]", "astype(np.float64)[np.asarray(codes) ^ 8]"),
     "codebook_layout_elements_swapped": ("nib_shift = (8 * reg + 4 * elem)", "nib_shift = (8 * reg + 4 * (1 - elem))"),
     "codebook_layout_registers_as_plain": ("nib_shift = (8 * reg + 4 * elem)", "nib_shift = (16 * elem + 4 * reg)"),
+    "rows_top_bits_table_permuted": ("TOP2_POS = (4, 8, 0, 12, 20, 24, 16, 28)", "TOP2_POS = (0, 8, 4, 12, 16, 24, 20, 28)"),
+    "rows_second_word_offset_dropped": ("2 * (j[:, None] % 2)", "0 * (j[:, None] % 2)"),
+    "rows_scale_block_row_major": ("reshape(ng, R)", "reshape(R, ng).T.reshape(ng, R)"),
+    "rows_chunk_and_row_swapped": ('reshape(C, R, 4)\n', 'reshape(R, C, 4).transpose(1, 0, 2)\n'),
     "bias_scaled_by_row_scale": ("y64 = y64 + (b if cols is None else b[np.asarray(cols)])[None, :]",
                                  "y64 = y64 + s[:, None] * (b if cols is None else b[np.asarray(cols)])[None, :]"),
 }
 
 PINS = ["hand_example", "file_layout", "forward_bruteforce", "quantize", "prologues",
-        "closed_forms", "invariants", "stream_positions", "stream_bijection", "stream_positions_codebook", "bias",
+        "closed_forms", "invariants", "stream_positions", "stream_bijection", "stream_positions_codebook", "stream_positions_rows", "bias",
         "moe", "codebook", "float_sanity"]
 
 

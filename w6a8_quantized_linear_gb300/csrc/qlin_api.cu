@@ -16,11 +16,13 @@
 
 #include "qlin.h"
 #include "qlin_forward.cuh"
+#include "qlin_forward_tc.cuh"
 #include "qlin_instances.h"
 #include "qlin_repack.cuh"
 
 // the forward kernels live in the qlin_kernels_*.cu translation units
 QLIN_KERNELS_ALL(QLIN_DECLARE_EXTERN)
+QLIN_TC_ALL(QLIN_TC_DECLARE_EXTERN)
 
 using namespace qlin;
 
@@ -117,6 +119,24 @@ const void* forward_fn(int bits, int64_t G, int mode = 0) {
                      : forward_fn_t<0>(bits, G);
 }
 
+// The tcgen05 kernel for a format and group size (G >= 32), modes 0 and 3.
+template <int BITS, int MODE>
+const void* tc_fn_g(int64_t G) {
+  switch (G) {
+    case 32: return reinterpret_cast<const void*>(qlin_tc_kernel<BITS, 32, MODE>);
+    case 64: return reinterpret_cast<const void*>(qlin_tc_kernel<BITS, 64, MODE>);
+    case 128: return reinterpret_cast<const void*>(qlin_tc_kernel<BITS, 128, MODE>);
+    case 256: return reinterpret_cast<const void*>(qlin_tc_kernel<BITS, 256, MODE>);
+    default: return nullptr;
+  }
+}
+const void* tc_fn(int bits, int64_t G, int mode) {
+  if (mode != 0 && mode != 3) return nullptr;
+  if (bits == 6) return mode == 3 ? tc_fn_g<6, 3>(G) : tc_fn_g<6, 0>(G);
+  return mode == 3 ? tc_fn_g<4, 3>(G) : tc_fn_g<4, 0>(G);
+}
+
+
 // Per-device set-up: SM count, and the kernel attributes every launch relies on
 // (large dynamic shared memory, clusters of up to 16 CTAs).  Caller holds g_mu.
 qlin_status device_cache(DevCache** out) {
@@ -137,6 +157,12 @@ qlin_status device_cache(DevCache** out) {
           if (e != cudaSuccess) return cuda_status(e);
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
           if (e != cudaSuccess) return cuda_status(e);
+          const void* tfn = G >= 32 ? tc_fn(bits, G, mode) : nullptr;
+          if (!tfn) continue;
+          e = cudaFuncSetAttribute(tfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
+          if (e != cudaSuccess) return cuda_status(e);
+          e = cudaFuncSetAttribute(tfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+          if (e != cudaSuccess) return cuda_status(e);
         }
     c.init = true;
   }
@@ -147,9 +173,9 @@ qlin_status device_cache(DevCache** out) {
 // Shared-memory carve: [extra][stages][activation operand][split-K slots]
 // (extra: the codebook table, which the kernel expects at offset 0).  Fails
 // when the budget holds fewer than min_stages stages (or the CTA's units).
-bool carve(const Geo& g, int64_t bbf, Plan& pl, int64_t budget, int64_t min_stages, int64_t extra) {
+bool carve(const Geo& g, int64_t bbf, Plan& pl, int64_t budget, int64_t min_stages, int64_t extra, bool tc = false) {
   pl.stage_bytes = round_up(2 * g.unit_full, 128);
-  const int64_t b_bytes = round_up(pl.upc * bbf, 128);
+  const int64_t b_bytes = round_up(pl.upc * bbf + (tc ? TC_B_HEAD + TC_B_TAIL : 0), 128);
   const int64_t cmax = (CONSUMERS + pl.C - 1) / pl.C;
   const int64_t red_bytes = round_up((int64_t)pl.C * cmax * 8 * 4, 128);
   const int64_t rest = b_bytes + red_bytes + extra + 128;
@@ -166,13 +192,13 @@ bool carve(const Geo& g, int64_t bbf, Plan& pl, int64_t budget, int64_t min_stag
 
 // Clusters of C CTAs (each with `smem` dynamic bytes) that the device holds at
 // once, from the occupancy query; cached per (kernel, C, smem).  Caller holds g_mu.
-int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
+int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem, int threads) {
   const auto key = std::make_pair(std::make_pair(fn, C), smem);
   auto it = dc.clusters.find(key);
   if (it != dc.clusters.end()) return it->second;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)C, 1, 1);
-  cfg.blockDim = dim3(GEMV_THREADS, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -199,17 +225,18 @@ int active_clusters(DevCache& dc, const void* fn, int C, int64_t smem) {
 // and of the RMSNorm statistics -- is the same for every M; plan_for_rows
 // then re-carves only the ring stages for the launch's rows.  Plans are
 // cached per launch geometry.  Caller holds g_mu.
-qlin_status make_plan(const Geo& g, int64_t NB, DevCache& dc, int mode, Plan* out) {
+qlin_status make_plan(const Geo& g, int64_t NB, DevCache& dc, int mode, bool tc, Plan* out) {
   // the test-hook mode computes exactly what the plain mode does, so it is
   // planned as the plain kernel (same C, same order of the sums)
-  const void* fn = forward_fn(g.bits, g.G, mode == 3 ? 0 : mode);
+  const void* fn = tc ? tc_fn(g.bits, g.G, mode == 3 ? 0 : mode) : forward_fn(g.bits, g.G, mode == 3 ? 0 : mode);
+  const int threads = tc ? TC_THREADS : GEMV_THREADS;
   const PlanKey key{fn, g.K, g.G, NB};
   auto it = dc.plans.find(key);
   if (it != dc.plans.end()) {
     *out = it->second;
     return QLIN_OK;
   }
-  const int64_t bbf = bblock_bytes(g.KB, g.G, MAX_M);
+  const int64_t bbf = tc ? tc_bblock_bytes(g.KB, g.G) : bblock_bytes(g.KB, g.G, MAX_M);
   const int64_t upc_cap = MAX_K_PER_CTA / g.KB;
   const int64_t cmin = (g.J + upc_cap - 1) / upc_cap;
   const int64_t cmax = g.J < MAX_CLUSTER ? g.J : MAX_CLUSTER;
@@ -224,9 +251,9 @@ qlin_status make_plan(const Geo& g, int64_t NB, DevCache& dc, int mode, Plan* ou
     pl.upc = (int)((g.J + c - 1) / c);
     // two CTAs per SM need at least two stages each (four units in flight per
     // SM keep DRAM busy); with fewer, one CTA per SM gets the whole budget
-    pl.alone = !carve(g, bbf, pl, SMEM_TWO_PER_SM, 2, extra);
-    if (pl.alone && !carve(g, bbf, pl, SMEM_MAX, 2, extra)) continue;
-    const int n = active_clusters(dc, fn, pl.C, pl.smem);
+    pl.alone = !carve(g, bbf, pl, SMEM_TWO_PER_SM, 2, extra, tc);
+    if (pl.alone && !carve(g, bbf, pl, SMEM_MAX, 2, extra, tc)) continue;
+    const int n = active_clusters(dc, fn, pl.C, pl.smem, threads);
     if (n < 1) continue;
     const int64_t cost = (NB + n - 1) / n * pl.upc;
     if (!found || cost < best_cost) {
@@ -243,9 +270,9 @@ qlin_status make_plan(const Geo& g, int64_t NB, DevCache& dc, int mode, Plan* ou
 // The plan for a launch of M rows: the cluster size of the MAX_M plan, with
 // the ring re-carved in the same budget for the (smaller or equal) operand
 // of M rows.  Stages change no summation order.
-Plan plan_for_rows(const Geo& g, const Plan& at_max, int M, int mode) {
+Plan plan_for_rows(const Geo& g, const Plan& at_max, int M, int mode, bool tc) {
   Plan pl = at_max;
-  if (M < MAX_M) {
+  if (M < MAX_M && !tc) {  // (the tcgen05 operand does not depend on M)
     const int64_t extra = mode == 2 ? CODEBOOK_LUT_BYTES : 0;
     Plan r = at_max;
     if (carve(g, bblock_bytes(g.KB, g.G, M), r, at_max.alone ? SMEM_MAX : SMEM_TWO_PER_SM, 2, extra)) pl = r;
@@ -321,7 +348,7 @@ struct Outputs {  // test exports of a single-weight call
 // NB_plan the row blocks its cluster size is chosen for (the same for every
 // M: NB itself for a weight table, the most experts an expert bank can route).
 qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, int64_t G, int64_t NB,
-                            int64_t NB_plan, const void* x, const void* gate, const void* up, const float* gamma, float eps,
+                            int64_t NB_plan, bool tc, const void* x, const void* gate, const void* up, const float* gamma, float eps,
                             const Outputs& out, void* ws, unsigned flags, void* stream, int64_t fault_unit) {
   const Geo g = make_geo(fmt, 0, K, G);  // the K geometry every weight shares
   const bool test_hooks = out.acc || out.q || out.s || fault_unit >= 0;
@@ -332,10 +359,10 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
     DevCache* dc = nullptr;
     qlin_status st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, NB_plan, *dc, mode, &pl);
+    st = make_plan(g, NB_plan, *dc, mode, tc, &pl);
     if (st != QLIN_OK) return st;
   }
-  pl = plan_for_rows(g, pl, M, mode);
+  pl = plan_for_rows(g, pl, M, mode, tc);
   pl.NB = NB;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.gate = static_cast<const __nv_bfloat16*>(gate);
@@ -362,9 +389,9 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
   p.fault_unit = fault_unit;
   p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
   void* args[] = {&p};
-  return launch(forward_fn(g.bits, G, mode), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
-                dim3(GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args, pl.C,
-                (flags & QLIN_FLAG_PDL) != 0);
+  return launch(tc ? tc_fn(g.bits, G, mode) : forward_fn(g.bits, G, mode), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
+                dim3(tc ? TC_THREADS : GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args,
+                pl.C, (flags & QLIN_FLAG_PDL) != 0);
 }
 
 // One launch over n weights that share the format, K, G and the activation
@@ -373,7 +400,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
                          const void* const* packed, const void* x, const void* gate, const void* up,
                          const float* gamma, float eps, float* const* ys, const float* const* biases,
                          const Outputs& out, void* ws, size_t ws_bytes, unsigned flags, void* stream, bool debug,
-                         int64_t fault_unit = -1, const float* codebook = nullptr) {
+                         int64_t fault_unit = -1, const float* codebook = nullptr, bool tc = false) {
   if (n < 1 || n > MAX_LIN || !Ns || !packed || !ys) return QLIN_ERR_INVALID_ARG;
   qlin_status st = QLIN_OK;
   int64_t NB = 0;
@@ -411,7 +438,7 @@ qlin_status forward_impl(int fmt, int kind, int M, int n, const int64_t* Ns, int
   }
   p.n_lin = nl;
   p.codebook = codebook;
-  return plan_and_launch(p, fmt, kind, M, K, G, NB, NB, x, gate, up, gamma, eps, out, ws, flags, stream,
+  return plan_and_launch(p, fmt, kind, M, K, G, NB, NB, tc, x, gate, up, gamma, eps, out, ws, flags, stream,
                          fault_unit);
 }
 
@@ -449,7 +476,7 @@ qlin_status moe_impl(int fmt, int kind, int M, int E, int64_t N, int64_t K, int6
   // depend on how many other tokens share the launch)
   const int64_t slots = std::min<int64_t>(E, (int64_t)M * topk);
   const int64_t slots_plan = std::min<int64_t>(E, (int64_t)MAX_M * topk);
-  return plan_and_launch(p, fmt, kind, M, K, G, slots * p.nbe, slots_plan * p.nbe, x, gate, up, gamma, eps,
+  return plan_and_launch(p, fmt, kind, M, K, G, slots * p.nbe, slots_plan * p.nbe, false, x, gate, up, gamma, eps,
                          Outputs(), ws, flags, stream, -1);
 }
 
@@ -530,7 +557,7 @@ qlin_status qlin_repack_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t G
 
 namespace {
 qlin_status repack_impl(int fmt, int64_t N, int64_t K, int64_t G, void* buf, void* ws, size_t ws_bytes,
-                        void* stream, bool cb_layout) {
+                        void* stream, int layout) {
   qlin_status st = check_shape_impl(fmt, N, K, G);
   if (st != QLIN_OK) return st;
   if (N == 0) return QLIN_OK;
@@ -558,7 +585,7 @@ qlin_status repack_impl(int fmt, int64_t N, int64_t K, int64_t G, void* buf, voi
   rp.stage = w + sc;
   rp.scales = reinterpret_cast<const float*>(w);
   rp.bits = g.bits;
-  rp.cb_layout = cb_layout ? 1 : 0;
+  rp.layout = layout;
   rp.N = N;
   rp.K = K;
   rp.G = G;
@@ -585,12 +612,12 @@ qlin_status repack_impl(int fmt, int64_t N, int64_t K, int64_t G, void* buf, voi
 
 qlin_status qlin_repack(int fmt, int64_t N, int64_t K, int64_t G, void* buf, void* ws, size_t ws_bytes,
                         void* stream) {
-  return repack_impl(fmt, N, K, G, buf, ws, ws_bytes, stream, false);
+  return repack_impl(fmt, N, K, G, buf, ws, ws_bytes, stream, LAYOUT_FRAGMENT);
 }
 
 qlin_status qlin_repack_codebook(int64_t N, int64_t K, int64_t G, void* buf, void* ws, size_t ws_bytes,
                                  void* stream) {
-  return repack_impl(QLIN_W4A8, N, K, G, buf, ws, ws_bytes, stream, true);
+  return repack_impl(QLIN_W4A8, N, K, G, buf, ws, ws_bytes, stream, LAYOUT_CODEBOOK);
 }
 
 qlin_status qlin_forward_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t G, size_t* bytes) {
@@ -654,7 +681,7 @@ qlin_status qlin_forward_launch_info(int fmt, int64_t N, int64_t K, int64_t G, i
     DevCache* dc = nullptr;
     st = device_cache(&dc);
     if (st != QLIN_OK) return st;
-    st = make_plan(g, row_blocks(N), *dc, 0, &pl);
+    st = make_plan(g, row_blocks(N), *dc, 0, false, &pl);
     if (st != QLIN_OK) return st;
   }
   *ctas = (int64_t)pl.C * pl.NB;
@@ -691,6 +718,29 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
   if (unit < 0) return QLIN_ERR_INVALID_ARG;
   return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, nullptr, Outputs(), ws,
                       ws_bytes, 0, stream, false, unit);
+}
+
+qlin_status qlin_debug_repack_tcgen05(int fmt, int64_t N, int64_t K, int64_t G, void* buf, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  qlin_status st = check_shape_impl(fmt, N, K, G);
+  if (st != QLIN_OK) return st;
+  if (G < 32) return QLIN_ERR_UNSUPPORTED;
+  return repack_impl(fmt, N, K, G, buf, ws, ws_bytes, stream, LAYOUT_ROWS);
+}
+
+qlin_status qlin_debug_forward_tcgen05(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,
+                                       const void* packed, const void* x, const void* gate, const void* up,
+                                       const float* gamma, float eps, float* y, int32_t* acc, int8_t* q, float* s,
+                                       void* ws, size_t ws_bytes, unsigned flags, void* stream) {
+  qlin_status st = check_shape_impl(fmt, N, K, G);
+  if (st != QLIN_OK) return st;
+  if (G < 32) return QLIN_ERR_UNSUPPORTED;
+  Outputs o;
+  o.acc = acc;
+  o.q = q;
+  o.s = s;
+  return forward_impl(fmt, prologue, M, 1, &N, K, G, &packed, x, gate, up, gamma, eps, &y, nullptr, o, ws, ws_bytes,
+                      flags, stream, false, -1, nullptr, true);
 }
 
 qlin_status qlin_forward_noalloc(int fmt, int prologue, int M, int64_t N, int64_t K, int64_t G,

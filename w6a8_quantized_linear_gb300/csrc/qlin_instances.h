@@ -19,6 +19,15 @@
   QLIN_KERNELS_W4(X) QLIN_KERNELS_W6(X) QLIN_KERNELS_CODEBOOK(X) QLIN_KERNELS_MOE_W4(X) QLIN_KERNELS_MOE_W6(X) \
   QLIN_KERNELS_EXPORT_W4(X) QLIN_KERNELS_EXPORT_W6(X)
 
+// The tcgen05 main loop (qlin_tc_kernel): groups of 32 k and more, the weight
+// table without (mode 0) and with (mode 3) the test hooks.
+#define QLIN_TC_KERNELS(X) X(4, 32, 0) X(4, 64, 0) X(4, 128, 0) X(4, 256, 0) X(6, 32, 0) X(6, 64, 0) X(6, 128, 0) X(6, 256, 0)
+#define QLIN_TC_KERNELS_EXPORT(X) \
+  X(4, 32, 3) X(4, 64, 3) X(4, 128, 3) X(4, 256, 3) X(6, 32, 3) X(6, 64, 3) X(6, 128, 3) X(6, 256, 3)
+#define QLIN_TC_ALL(X) QLIN_TC_KERNELS(X) QLIN_TC_KERNELS_EXPORT(X)
+
 #define QLIN_INSTANTIATE(B, G, M) template __global__ void qlin::qlin_forward_kernel<B, G, M>(qlin::FwdParams);
 #define QLIN_DECLARE_EXTERN(B, G, M) \
   extern template __global__ void qlin::qlin_forward_kernel<B, G, M>(qlin::FwdParams);
+#define QLIN_TC_INSTANTIATE(B, G, M) template __global__ void qlin::qlin_tc_kernel<B, G, M>(qlin::FwdParams);
+#define QLIN_TC_DECLARE_EXTERN(B, G, M) extern template __global__ void qlin::qlin_tc_kernel<B, G, M>(qlin::FwdParams);

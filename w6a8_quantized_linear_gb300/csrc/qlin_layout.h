@@ -100,6 +100,11 @@ QL_HD int64_t unit_offset(const Geo& g, int64_t t, int64_t j) {
   return t * g.tile_full + j * unit_bytes(g.bits, tile_rows(g, t), g.KB, g.G);
 }
 
+// Stream layouts of the code block of a unit (documented with qlin_repack in
+// qlin.h): the warp-fragment order of the mma.sync main loop, its codebook
+// variant, and the row order of the tcgen05 main loop.
+constexpr int LAYOUT_FRAGMENT = 0, LAYOUT_CODEBOOK = 1, LAYOUT_ROWS = 2;
+
 // K split inside a cluster of C CTAs: rank c owns stream units [c*J/C, (c+1)*J/C).
 QL_HD int64_t split_begin(int64_t c, int64_t J, int64_t C) { return c * J / C; }
 

@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
                                                   vp, sz, i64, vp]),
                 "qlin_forward_noalloc": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp,
                                               ctypes.c_uint, vp]),
+                "qlin_debug_repack_tcgen05": (st, [i32, i64, i64, i64, vp, vp, sz, vp]),
+                "qlin_debug_forward_tcgen05": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float,
+                                                    vp, vp, vp, vp, vp, sz, ctypes.c_uint, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -314,3 +317,36 @@ def debug_forward_fault(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: 
     return lib().qlin_debug_forward_fault(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate),
                                           _ptr(up), _ptr(gamma), float(eps), _ptr(y), _ptr(ws), ws.numel(), unit,
                                           _stream(stream))
+
+
+def debug_repack_tcgen05(buf: torch.Tensor, fmt, N: int, K: int, G: int, ws: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """``repack`` into the row layout of the tcgen05 main loop (test export; G >= 32)."""
+    if ws is None:
+        _, rec = repack_workspace_bytes(fmt, N, K, G)
+        ws = torch.empty(rec, dtype=torch.uint8, device=buf.device)
+    _check(lib().qlin_debug_repack_tcgen05(_fmt(fmt), N, K, G, _ptr(buf), _ptr(ws), ws.numel(), _stream(stream)),
+           "debug_repack_tcgen05")
+    return buf
+
+
+def debug_forward_tcgen05(fmt, prologue, packed: torch.Tensor, N: int, K: int, G: int, x=None, gate=None, up=None,
+                          gamma=None, eps: float = 1e-6, y: torch.Tensor | None = None, exports: bool = False,
+                          ws: torch.Tensor | None = None, flags: int = 0, stream=None) -> dict:
+    """The tcgen05 main loop on a weight from ``debug_repack_tcgen05`` (test
+    export): y, and with ``exports`` the exact group sums, codes and row scales."""
+    act = gate if _pro(prologue) == 2 else x
+    M = act.shape[0]
+    dev = packed.device
+    out = {"y": y if y is not None else torch.empty(M, N, dtype=torch.float32, device=dev)}
+    if exports:
+        out["acc"] = torch.empty(M, N, K // G, dtype=torch.int32, device=dev)
+        out["q"] = torch.empty(M, K, dtype=torch.int8, device=dev)
+        out["s"] = torch.empty(M, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = new_workspace(forward_workspace_bytes(fmt, N, K, G), dev, stream)
+    _check(lib().qlin_debug_forward_tcgen05(_fmt(fmt), _pro(prologue), M, N, K, G, _ptr(packed), _ptr(x), _ptr(gate),
+                                            _ptr(up), _ptr(gamma), float(eps), _ptr(out["y"]), _ptr(out.get("acc")),
+                                            _ptr(out.get("q")), _ptr(out.get("s")), _ptr(ws), ws.numel(), flags,
+                                            _stream(stream)), "debug_forward_tcgen05")
+    return out
