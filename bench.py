@@ -650,6 +650,8 @@ def main():
     ap.add_argument("--config", default=None, help="profile mode: one single-linear benchmark configuration")
     ap.add_argument("--moe", action="store_true", help="profile mode: the expert-bank launch")
     ap.add_argument("--print-kernel-hash", action="store_true")
+    ap.add_argument("--stack-only", action="store_true",
+                    help="time the stack only (no widened paths, no per-configuration lines)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -704,8 +706,8 @@ def main():
             e["bytes_per_launch"] = nbytes // n
             del g
 
-    widened = next_rows(stack, stream, max(3, args.steps // 2), peak)
-    per_config = config_lines(dev, stream, max(3, args.steps // 4), peak)
+    widened = next_rows(stack, stream, max(3, args.steps // 2), peak) if not args.stack_only else None
+    per_config = config_lines(dev, stream, max(3, args.steps // 4), peak) if not args.stack_only else None
 
     # end to end through the public call with host buffers: pinned host
     # activations in, every call's output back, each step
