@@ -156,6 +156,7 @@ def max_over_ranks(v: float, ws: int, device) -> float:
 KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
 TRAFFIC = {
     "0f3f5b1ea3945020": {"bytes_per_launch": 97141248},
+    "2c2b2c737308ed6d": {"bytes_per_launch": 97567488},
 }
 TRAFFIC_METRICS = "ncu dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch"
 
@@ -228,9 +229,10 @@ class Stack:
         self.ws = qlin.new_workspace(nbytes, device)
         torch.cuda.synchronize(device)
 
-    def groups(self, M: int):
-        """(group name, prologue, [names], K, [N], [packed], x, gate, up, gamma, [y]) per launch group of a step."""
-        a_off = o_off = 0
+    def groups(self, M: int, a_base: int = 0, o_base: int = 0):
+        """(group name, prologue, [names], K, [N], [packed], x, gate, up, gamma, [y]) per launch group of a step
+        (activations from element a_base of the flat activation buffer, outputs from o_base)."""
+        a_off, o_off = a_base, o_base
         out = []
         for l in range(self.layers):
             for gname, kind, names in self.GROUPS:
@@ -265,10 +267,10 @@ class Stack:
                          flags=qlin.FLAG_PDL, stream=stream)
         return len(names)
 
-    def graph(self, M: int, stream, grouped: bool = True, only: str | None = None):
+    def graph(self, M: int, stream, grouped: bool = True, only: str | None = None, a_base: int = 0, o_base: int = 0):
         """One CUDA graph of a step (or of one launch group across all layers)."""
         import torch
-        grps = [g for g in self.groups(M) if only is None or g[0] == only]
+        grps = [g for g in self.groups(M, a_base, o_base) if only is None or g[0] == only]
         for grp in grps[:4]:  # plans are made outside capture
             self.launch(grp, stream, grouped)
         torch.cuda.synchronize(self.dev)
@@ -709,62 +711,80 @@ def main():
     widened = next_rows(stack, stream, max(3, args.steps // 2), peak) if not args.stack_only else None
     per_config = config_lines(dev, stream, max(3, args.steps // 4), peak) if not args.stack_only else None
 
-    # end to end through the public call with host buffers: pinned host
-    # activations in, every call's output back, each step
-    d_act = stack.act[:stack.act_per_row]   # the M = 1 step's inputs
-    d_out = stack.out[:stack.out_per_row]   # and its outputs
-    h_act = torch.empty(d_act.numel(), dtype=torch.bfloat16, pin_memory=True)
-    h_act.copy_(d_act)
-    h_out = torch.empty(d_out.numel(), dtype=torch.float32, pin_memory=True)
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            d_act.copy_(h_act, non_blocking=True)
-            g1.replay()
-            h_out.copy_(d_out, non_blocking=True)
-    torch.cuda.synchronize()
+    # End to end through the public call with host buffers: every step copies
+    # its activations in from pinned host memory and every call's output back.
+    # Two buffer sets (the M = 1 step's inputs and outputs, and a second copy
+    # of them) let the copies of one step overlap the compute of the next, as
+    # a serving loop pipelines them: step i's inputs go in on one copy stream
+    # once step i - 2 has finished with that set, step i runs when they have
+    # landed, and its outputs come back on another copy stream.
+    A, O_ = stack.act_per_row, stack.out_per_row
+    sets = [(stack.act[:A], stack.out[:O_], g1), (stack.act[A:2 * A], stack.out[O_:2 * O_], stack.graph(1, stream, a_base=A, o_base=O_)[0])]
+    h_act = torch.empty(A, dtype=torch.bfloat16, pin_memory=True)
+    h_act.copy_(stack.act[:A])
+    h_out = [torch.empty(O_, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def pipelined(n, step_fn):
+        comp_done = [torch.cuda.Event() for _ in range(2)]
+        out_read = [torch.cuda.Event() for _ in range(2)]
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(h2d)
+        for i in range(n):
+            k = i % 2
+            d_act, d_out, g = sets[k]
+            with torch.cuda.stream(h2d):
+                if i >= 2:
+                    h2d.wait_event(comp_done[k])
+                d_act.copy_(h_act, non_blocking=True)
+                in_ready[k].record(h2d)
+            stream.wait_event(in_ready[k])
+            if i >= 2:
+                stream.wait_event(out_read[k])
+            with torch.cuda.stream(stream):
+                step_fn(k, g)
+                comp_done[k].record(stream)
+            d2h.wait_event(comp_done[k])
+            with torch.cuda.stream(d2h):
+                h_out[k].copy_(d_out, non_blocking=True)
+                out_read[k].record(d2h)
+        e1.record(d2h)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def graph_step(k, g):
+        g.replay()
+
+    pipelined(args.warmup, graph_step)
     barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            d_act.copy_(h_act, non_blocking=True)
-            g1.replay()
-            h_out.copy_(d_out, non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    te2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    te2e = max_over_ranks(pipelined(args.steps, graph_step), world, dev)
     gbs_e2e = job_gbs(world, wb, te2e)
+    # the outputs that came back are the step's: the last copy of each set
+    # equals what the device holds
+    assert torch.equal(h_out[(args.steps - 1) % 2], sets[(args.steps - 1) % 2][1].cpu())
 
     # the same end to end without a graph: each step's launches enqueued call
     # by call through the binding (the C ABI underneath), as an application
     # that does not capture graphs runs them
-    grps1 = stack.groups(1)
+    grp_sets = [stack.groups(1), stack.groups(1, A, O_)]
+    n_eager = len(grp_sets[0])  # one launch per group (q/k/v and gate/up as multi-weight launches)
 
-    def eager_step():
-        d_act.copy_(h_act, non_blocking=True)
-        n = 0
-        for grp in grps1:
-            n += stack.launch(grp, stream, True)
-        h_out.copy_(d_out, non_blocking=True)
-        return n
+    def eager_step(k, g):
+        for grp in grp_sets[k]:
+            stack.launch(grp, stream, True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            eager_step()
+    pipelined(args.warmup, eager_step)
+    host_us = []  # host time to enqueue one step's launches, from an idle queue
+    for _ in range(5):
         torch.cuda.synchronize()
-        host_us = []  # host time to enqueue one step, from an idle queue
-        for _ in range(5):
-            t0 = time.perf_counter()
-            n_eager = eager_step()
-            host_us.append((time.perf_counter() - t0) * 1e6 / n_eager)
-            torch.cuda.synchronize()
-        barrier(world)
-        e0.record(stream)
-        for _ in range(args.steps):
-            eager_step()
-        e1.record(stream)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            eager_step(0, None)
+        host_us.append((time.perf_counter() - t0) * 1e6 / n_eager)
     torch.cuda.synchronize()
-    te2e_eager = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    barrier(world)
+    te2e_eager = max_over_ranks(pipelined(args.steps, eager_step), world, dev)
 
     assert qlin.read_device_status(stack.ws) == qlin.OK
 
@@ -810,10 +830,11 @@ def main():
                                         else f"kernel sources {kernel_hash()} changed since the last ncu capture")},
         "cpu_baseline": cpu,
         "e2e": {"value": gbs_e2e, "unit": "GB/s", "ms_per_step": te2e,
-                "h2d_bytes_per_step": h_act.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 4},
+                "h2d_bytes_per_step": h_act.numel() * 2, "d2h_bytes_per_step": h_out[0].numel() * 4,
+                "pipelining": "two buffer sets; step i+1's inputs copied in while step i computes"},
         "e2e_eager": {"value": job_gbs(world, wb, te2e_eager), "unit": "GB/s", "ms_per_step": te2e_eager,
                       "launches_per_step": n_eager, "host_us_per_call": statistics.median(host_us),
-                      "h2d_bytes_per_step": h_act.numel() * 2, "d2h_bytes_per_step": h_out.numel() * 4},
+                      "h2d_bytes_per_step": h_act.numel() * 2, "d2h_bytes_per_step": h_out[0].numel() * 4},
         "gpu_launches": ncalls * args.steps,
         "clocks": clocks,
         # the second half of the headline, last on the line
