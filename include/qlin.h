@@ -315,6 +315,14 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
                                      int64_t unit, void* stream);
 
 /*
+ * Test export: the plan qlin_forward uses on the current device for a weight
+ * of N rows, K columns and group size G at M rows: *cluster = CTAs that split
+ * K for one 256-row block (the same for every M), *stages = ring stages per
+ * CTA (more for fewer rows, whose activation operand is smaller).
+ */
+qlin_status qlin_debug_plan(int fmt, int M, int64_t N, int64_t K, int64_t G, int* cluster, int* stages);
+
+/*
  * Test exports of the second main loop, on the 5th-generation tensor cores
  * (tcgen05.mma with the fp16 weight operand in tensor memory, accumulators in
  * tensor memory), kept to measure it against qlin_forward's warp-level MMA

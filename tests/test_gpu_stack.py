@@ -17,6 +17,8 @@ that do not depend on M.
   for 8 rows whatever M is ("Doubling the LLM token rate in ComfyUI",
   section "Optimising the linear kernel": up to eight rows of MTP drafts run
   at the cost of one).
+* The plan of each benchmark shape: the same cluster size for every M, and
+  each shape against the oracle in its plan at M = 8, rows independent of M.
 """
 import numpy as np
 import pytest
@@ -144,3 +146,46 @@ def test_rows_bit_identical_across_m(name):
             assert torch.equal(full[r:r + 1], one), f"{name}: weight {l}, row {r} alone"
     for l, y in enumerate(y8):
         assert torch.isfinite(y).all() and y.abs().max() > 0, f"{name}: weight {l} output"
+
+
+# ------------------------------------------------------------ plans of the benchmark shapes
+PLAN_SHAPES = [("w4a8", 6144, 5120, 128), ("w4a8", 5120, 6144, 128), ("w4a8", 17408, 5120, 128),
+               ("w4a8", 5120, 17408, 128), ("w4a8", 4096, 4096, 128), ("w4a8", 4096, 12288, 128),
+               ("w6a8", 17408, 5120, 32), ("w6a8", 5120, 17408, 32)]
+
+
+def test_plans_keep_their_cluster_size_for_every_m():
+    """The cluster size (the split of K, and so the order of every fp32 sum)
+    is the same for M = 1..8; fewer rows may only deepen the ring."""
+    for fmt, N, K, G in PLAN_SHAPES:
+        plans = [qlin.debug_plan(fmt, M, N, K, G) for M in range(1, 9)]
+        assert len({p["cluster"] for p in plans}) == 1, (fmt, N, K, G, plans)
+        stages = [p["stages"] for p in plans]
+        assert stages == sorted(stages, reverse=True) and stages[-1] >= 1, (fmt, N, K, G, plans)
+
+
+@pytest.mark.parametrize("fmt,N,K,G", PLAN_SHAPES)
+def test_planned_shape_matches_oracle_and_rows_are_independent_of_m(fmt, N, K, G):
+    """Each benchmark shape in its plan at M = 8: y against the oracle on
+    sampled columns (the exact group sums too, for the codes the kernel
+    chose), and rows 0 and 6 of the 8-row call equal to those rows alone."""
+    kind = "rmsnorm" if K <= 6144 else "swiglu"
+    c = inputs.make_case(fmt, kind, 8, N, K, G, seed=N ^ K, scale_range=(0.002, 0.01))
+    d = device_case(c)
+    y8 = qlin.forward(fmt, kind, d["w"], N, K, G, flags=qlin.FLAG_PDL, **acts(c, d))
+    r = qlin.debug_forward(fmt, kind, d["w"], N, K, G, **acts(c, d))
+    assert torch.equal(y8, r["y"])
+    cols = sample_cols(N, 256, seed=7)
+    ref = oracle_forward(c, cols=cols)
+    assert_y_close(y8.cpu().numpy()[:, cols], ref["y64"], f"{fmt} {N}x{K} plan {qlin.debug_plan(fmt, 8, N, K, G)}")
+    qg = r["q"].cpu().numpy().astype(np.int64)
+    boundary_ok(qg, ref)
+    dq = (qg - ref["q"]).reshape(8, K // G, G)
+    codes, _ = O.unpack_file(fmt, N, K, G, c.wbuf.numpy(), rows=cols)
+    L = (codes - O.code_offset(fmt)).reshape(len(cols), K // G, G)
+    assert np.array_equal(r["acc"].cpu().numpy().astype(np.int64)[:, cols, :], ref["acc"] + np.einsum("mgk,ngk->mng", dq, L))
+    a = acts(c, d)
+    for m in (0, 6):
+        row = {k: (v[m:m + 1].contiguous() if k in ("x", "gate", "up") and v is not None else v) for k, v in a.items()}
+        one = qlin.forward(fmt, kind, d["w"], N, K, G, flags=qlin.FLAG_PDL, **row)
+        assert torch.equal(y8[m], one[0]), m

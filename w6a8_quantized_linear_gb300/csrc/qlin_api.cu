@@ -720,6 +720,26 @@ qlin_status qlin_debug_forward_fault(int fmt, int prologue, int M, int64_t N, in
                       ws_bytes, 0, stream, false, unit);
 }
 
+qlin_status qlin_debug_plan(int fmt, int M, int64_t N, int64_t K, int64_t G, int* cluster, int* stages) {
+  qlin_status st = check_shape_impl(fmt, N, K, G);
+  if (st != QLIN_OK) return st;
+  if (M < 1 || M > MAX_M || !cluster || !stages) return QLIN_ERR_INVALID_ARG;
+  const Geo g = make_geo(fmt, 0, K, G);
+  Plan pl;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevCache* dc = nullptr;
+    st = device_cache(&dc);
+    if (st != QLIN_OK) return st;
+    st = make_plan(g, row_blocks(N), *dc, 0, false, &pl);
+    if (st != QLIN_OK) return st;
+  }
+  pl = plan_for_rows(g, pl, M, 0, false);
+  *cluster = pl.C;
+  *stages = pl.stages;
+  return QLIN_OK;
+}
+
 qlin_status qlin_debug_repack_tcgen05(int fmt, int64_t N, int64_t K, int64_t G, void* buf, void* ws,
                                       size_t ws_bytes, void* stream) {
   qlin_status st = check_shape_impl(fmt, N, K, G);

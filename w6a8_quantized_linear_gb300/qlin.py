@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
                                                   vp, sz, i64, vp]),
                 "qlin_forward_noalloc": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float, vp,
                                               ctypes.c_uint, vp]),
+                "qlin_debug_plan": (st, [i32, i32, i64, i64, i64, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
                 "qlin_debug_repack_tcgen05": (st, [i32, i64, i64, i64, vp, vp, sz, vp]),
                 "qlin_debug_forward_tcgen05": (st, [i32, i32, i32, i64, i64, i64, vp, vp, vp, vp, vp, ctypes.c_float,
                                                     vp, vp, vp, vp, vp, sz, ctypes.c_uint, vp]),
@@ -350,3 +351,10 @@ def debug_forward_tcgen05(fmt, prologue, packed: torch.Tensor, N: int, K: int, G
                                             _ptr(out.get("q")), _ptr(out.get("s")), _ptr(ws), ws.numel(), flags,
                                             _stream(stream)), "debug_forward_tcgen05")
     return out
+
+
+def debug_plan(fmt, M: int, N: int, K: int, G: int) -> dict:
+    """The plan qlin_forward uses for this shape on the current device (test export)."""
+    c, st = ctypes.c_int(), ctypes.c_int()
+    _check(lib().qlin_debug_plan(_fmt(fmt), M, N, K, G, ctypes.byref(c), ctypes.byref(st)), "debug_plan")
+    return {"cluster": c.value, "stages": st.value}
