@@ -92,7 +92,7 @@ const void* fwd_fn_g(int gi) {
       case 3: return fwd_fn<BITS, 256, MODE>();
       default: break;
     }
-    if constexpr (MODE == 0 || MODE == 3) {
+    if constexpr (MODE == 0 || MODE == 3 || MODE == 4) {
       if (gi == 4) return fwd_fn<BITS, 16, MODE>();
       if constexpr (BITS == 4) {
         if (gi == 5) return fwd_fn<BITS, 8, MODE>();
@@ -116,6 +116,7 @@ const void* forward_fn(int bits, int64_t G, int mode = 0) {
   return mode == 1   ? forward_fn_t<1>(bits, G)
          : mode == 2 ? forward_fn_t<2>(bits, G)
          : mode == 3 ? forward_fn_t<3>(bits, G)
+         : mode == 4 ? forward_fn_t<4>(bits, G)
                      : forward_fn_t<0>(bits, G);
 }
 
@@ -150,7 +151,7 @@ qlin_status device_cache(DevCache** out) {
     if (e != cudaSuccess) return cuda_status(e);
     for (int bits : {4, 6})
       for (int64_t G : {4, 8, 16, 32, 64, 128, 256})
-        for (int mode = 0; mode < 4; mode++) {
+        for (int mode = 0; mode < 5; mode++) {
           const void* fn = forward_fn(bits, G, mode);
           if (!fn) continue;
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
@@ -389,7 +390,10 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
   p.fault_unit = fault_unit;
   p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
   void* args[] = {&p};
-  return launch(tc ? tc_fn(g.bits, G, mode) : forward_fn(g.bits, G, mode), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
+  // one activation row on the plain weight table: the kernel without the
+  // code of the wider prologues (planned, above, as the plain kernel)
+  const int launch_mode = (mode == 0 && M == 1) ? 4 : mode;
+  return launch(tc ? tc_fn(g.bits, G, mode) : forward_fn(g.bits, G, launch_mode), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
                 dim3(tc ? TC_THREADS : GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args,
                 pl.C, (flags & QLIN_FLAG_PDL) != 0);
 }

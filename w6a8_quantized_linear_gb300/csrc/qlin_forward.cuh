@@ -317,10 +317,13 @@ __device__ __forceinline__ void group_mma(const uint32_t (&a)[4], const uint32_t
 // MODE: 0 plain (weight table), 1 expert bank, 2 4-bit codebook levels,
 // 3 plain with the test hooks (activation codes, row scales and exact group
 // sums exported; one weight copy withheld), kept out of the other modes so
-// that their hot code stays compact.
+// that their hot code stays compact; 4 plain for one activation row only (the
+// decode step without drafts: its launches then carry none of the code of
+// the 2-, 4- and 8-row prologues, which costs a step measurably even when it
+// never runs).  Mode 4 computes exactly what mode 0 computes for M = 1.
 template <int BITS, int G, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
-  constexpr bool MOE = MODE == 1, CB = MODE == 2, EXPORT = MODE == 3;
+  constexpr bool MOE = MODE == 1, CB = MODE == 2, EXPORT = MODE == 3, ONE_ROW = MODE == 4;
   // dynamic shared memory: [codebook table (codebook mode)][stages][activation
   // operand][split-K slots]; the table sits first so that its address is a
   // constant of the kernel
@@ -735,7 +738,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   auto by_rows = [&](auto kind_tag) {
     // (the order of the cases sets the code layout, which measurably matters:
     // this one measured best for 1 and 8 rows together)
-    if (M > 4) {
+    if constexpr (ONE_ROW) {
+      prologue(kind_tag, IntTag<1>{});
+    } else if (M > 4) {
       prologue(kind_tag, IntTag<8>{});
     } else if (M <= 1) {
       prologue(kind_tag, IntTag<1>{});
