@@ -548,6 +548,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     constexpr bool REV = !MOE;
     const int rl = REV ? rounds - 1 : 0;
     ActSlice<KIND, MT> act;
+    // One-row mode: phase 1 keeps the prologue values of the round it reads
+    // last (round 0), and phase 2 quantises them without forming them again.
+    constexpr bool HOLDV = ONE_ROW && KIND != 2 && REV;
+    float hv[8];
     if (tid + (int64_t)rl * CONSUMERS < n8)
       act.load_gamma(p, k_lo + (tid + (int64_t)rl * CONSUMERS) * 8);  // a model parameter: may be read early
     pdl_wait();  // activations may be written by the previous kernel in the stream
@@ -569,6 +573,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
               act.value(m, v, ssq[m]);
   #pragma unroll
               for (int e = 0; e < 8; e++) amax[m] = fmaxf(amax[m], fabsf(v[e]));
+              if constexpr (HOLDV) {
+  #pragma unroll
+                for (int e = 0; e < 8; e++) hv[e] = v[e];
+              }
             }
           }
         }
@@ -608,10 +616,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         a = fmaxf(a, s_slot[r][tid][0]);
         q = __fadd_rn(q, s_slot[r][tid][1]);
       }
-      // Row scale s and the factor c that maps a prologue value to its code
-      // (a * c = a / s).  With no prologue s and the quotients are IEEE, so the
-      // codes equal the definition bit for bit; with a prologue the tolerance
-      // of the method allows the fast reciprocal forms.
+      // Row scale s and the factor c that maps a prologue value to its code.
+      // With no prologue s and the quotients are IEEE, so the codes equal the
+      // definition bit for bit; with a prologue the tolerance of the method
+      // allows a product by c, rounded once (see phase 2).
       float s, c;
       if (KIND == 0) {
         s = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
@@ -620,7 +628,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         const float rs = KIND == 1 ? rsqrtf(__fadd_rn(__fmul_rn(q, p.inv_k), p.eps)) : 1.0f;
         const float amax = __fmul_rn(a, rs);  // = max |fl(x*gamma) * rstd| (rounding is monotone)
         s = amax * (1.0f / 127.0f);
-        c = amax > 0.f ? __fmul_rn(rs, __fdividef(127.0f, amax)) : 0.f;
+        // the code of value v is v * rstd / s = v * 127 / a: rstd cancels, so
+        // c = 127 / a, correctly rounded (codes then differ from the exact
+        // quotient only within about an ulp of a rounding boundary)
+        c = a > 0.f ? __fdiv_rn(127.0f, a) : 0.f;
       }
       s_row[tid][0] = s;
       s_row[tid][1] = c;
@@ -658,19 +669,26 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
             float qf[8];
             if (valid) {
               float v[8], ss = 0.f;
-              act.value(m, v, ss);
+              if (HOLDV && r == 0) {
+  #pragma unroll
+                for (int e = 0; e < 8; e++) v[e] = hv[e];
+              } else {
+                act.value(m, v, ss);
+              }
               const float s = s_row[m][0], c = s_row[m][1];
               // |t| <= 127 (1 + a few ulp) because |a| <= amax, so round half to
               // even never leaves [-127, 127]: no clamp is needed
   #pragma unroll
               for (int e = 0; e < 8; e++) {
+                // round half to even: x + M - M with M = 1.5 * 2^23; with a
+                // prologue the product a * c is rounded once, by the fma
                 float t;
                 if (KIND == 0) {
-                  t = s > 0.f ? __fdiv_rn(v[e], s) : 0.f;  // IEEE division: codes identical to the definition
+                  t = __fadd_rn(s > 0.f ? __fdiv_rn(v[e], s) : 0.f, RINT_MAGIC);  // IEEE division: codes identical to the definition
                 } else {
-                  t = __fmul_rn(v[e], c);
+                  t = __fmaf_rn(v[e], c, RINT_MAGIC);
                 }
-                const float q = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);  // round half to even
+                const float q = __fsub_rn(t, RINT_MAGIC);
                 qf[e] = q;
                 rowsum[m] += q;
                 if (G == 4 && e < 4) rowlo[m] += q;

@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) qlin_tc_kernel(FwdParams p) {
         const float rs = KIND == 1 ? rsqrtf(__fadd_rn(__fmul_rn(q, p.inv_k), p.eps)) : 1.0f;
         const float amax = __fmul_rn(a, rs);
         s = amax * (1.0f / 127.0f);
-        c = amax > 0.f ? __fmul_rn(rs, __fdividef(127.0f, amax)) : 0.f;
+        c = a > 0.f ? __fdiv_rn(127.0f, a) : 0.f;  // rstd cancels from v * rstd / s (as in qlin_forward_kernel)
       }
       s_row[tid][0] = s;
       s_row[tid][1] = c;
@@ -378,13 +378,10 @@ __global__ void __launch_bounds__(TC_THREADS, 2) qlin_tc_kernel(FwdParams p) {
               const float s = s_row[m][0], cf = s_row[m][1];
 #pragma unroll
               for (int e = 0; e < 8; e++) {
-                float t;
-                if (KIND == 0) {
-                  t = s > 0.f ? __fdiv_rn(v[e], s) : 0.f;
-                } else {
-                  t = __fmul_rn(v[e], cf);
-                }
-                qf[e] = __fsub_rn(__fadd_rn(t, RINT_MAGIC), RINT_MAGIC);
+                // round half to even (the product a * c rounded once, as in qlin_forward_kernel)
+                const float t = KIND == 0 ? __fadd_rn(s > 0.f ? __fdiv_rn(v[e], s) : 0.f, RINT_MAGIC)
+                                          : __fmaf_rn(v[e], cf, RINT_MAGIC);
+                qf[e] = __fsub_rn(t, RINT_MAGIC);
               }
               if (EXPORT && p.q_out && blockIdx.y == 0) {
 #pragma unroll
