@@ -157,6 +157,7 @@ KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
 TRAFFIC = {
     "0f3f5b1ea3945020": {"bytes_per_launch": 97141248},
     "2c2b2c737308ed6d": {"bytes_per_launch": 97567488},
+    "2e15078fe7a49fc1": {"bytes_per_launch": 97483776},
 }
 TRAFFIC_METRICS = "ncu dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch"
 
@@ -823,7 +824,7 @@ def main():
         "per_config": per_config,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic["bytes_per_launch"] if traffic else None,
-                     "kernel": "qlin_forward_kernel<4,128,0> (RMSNorm prologue): the gate/up multi-weight launch, M=1, "
+                     "kernel": "qlin_forward_kernel<4,128,4> (the one-row variant; RMSNorm prologue): the gate/up multi-weight launch, M=1, "
                                f"{gu_bytes} algorithmic bytes per launch, {gu_us:.2f} us per launch (CUDA events, "
                                "64 launches in a graph)",
                      "traffic_source": (f"{TRAFFIC_METRICS}, kernel sources {kernel_hash()}" if traffic
