@@ -806,7 +806,11 @@ def main():
     traffic = kernel_traffic()
     line = {
         "metric": METRIC, "value": gbs1, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": t1, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": t1,
+        # the second half of the headline (the same stack at M=8), next to the first
+        "m8": {"value": gbs8, "ms_per_step": t8, "pct_of_hbm_peak": 100.0 * gbs8 / world / peak},
+        "t8_over_t1": t8 / t1,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8",
         "dtype_detail": "int8 activation codes x 4-bit weight levels, exact integer group sums (fp16 tensor-core "
                         "MMA on exact integers, fp32 accumulate), fp32 group and row scales, fp32 output",
@@ -814,7 +818,9 @@ def main():
         "config": {"workload": WORKLOAD, "M": 1, "layers": args.layers, "launches_per_step": ncalls,
                    "grouping": "q/k/v and gate/up as multi-weight launches sharing one prologue; o, down alone",
                    "weight_bytes_per_step": wb, "l2": "inputs larger than L2 (weights streamed once per step)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   # the metric is quoted at M=1 and M=8: the M=8 step of the same workload
+                   "m8": {"GB/s": gbs8, "ms_per_step": t8, "t8_over_t1": t8 / t1}},
         "pct_of_hbm_peak": 100.0 * gbs1 / world / peak, "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
         "pct_of_8tbs_spec": 100.0 * gbs1 / world / 8000.0,
         "separate_launches": {"launches_per_step": ncalls_sep, "value": job_gbs(world, wb, ts1),
@@ -838,9 +844,6 @@ def main():
                       "h2d_bytes_per_step": h_act.numel() * 2, "d2h_bytes_per_step": h_out[0].numel() * 4},
         "gpu_launches": ncalls * args.steps,
         "clocks": clocks,
-        # the second half of the headline, last on the line
-        "m8": {"value": gbs8, "ms_per_step": t8, "pct_of_hbm_peak": 100.0 * gbs8 / world / peak},
-        "t8_over_t1": t8 / t1,
     }
     if rank == 0:
         print(json.dumps(line))
