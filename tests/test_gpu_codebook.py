@@ -7,7 +7,9 @@ bits); the output tolerance of the method's benchmark statement covers that.
 Checked against the oracle's codebook definition: non-uniform tables, all
 prologues and group sizes, ragged N, bias, the uniform table against the
 plain path, exact power-of-two scaling, an all-zero table, and a full-size
-configuration on sampled columns.
+configuration on sampled columns.  Rows do not depend on M: each row of an
+8-row call equals that row run alone (bit for bit; a one-row launch runs the
+kernel compiled for one row).
 """
 import numpy as np
 import pytest
@@ -138,3 +140,17 @@ def test_codebook_full_size_sampled(M):
     cols = sample_cols(c.N, 256, seed=M)
     ref = _oracle(c, cb, cols=cols)
     assert_y_close(y.cpu().numpy()[:, cols], ref["y64"], f"full-size codebook M={M}")
+
+
+@pytest.mark.parametrize("kind,G", [("rmsnorm", 128), ("swiglu", 32), ("none", 64)])
+def test_codebook_row_alone_equals_row_in_batch(kind, G):
+    c = inputs.make_case("w4a8", kind, 8, 1040, 4096, G, seed=G + 3)
+    d = _device_cb(c)
+    cb = _table(G)
+    y8 = _run(c, d, cb)
+    for m in range(8):
+        dm = dict(d)
+        for k in ("x", "gate", "up"):
+            dm[k] = None if d[k] is None else d[k][m:m + 1].contiguous()
+        y1 = _run(c, dm, cb)  # (the rows come from the activation tensors)
+        assert torch.equal(y1[0], y8[m]), m

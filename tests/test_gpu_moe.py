@@ -6,6 +6,9 @@ section "Embeddings and MoE": expert and output rows flattened to E * N); ids
 against the oracle's expert-bank definition: duplicate experts in one token,
 ids outside [0, E) (rows left untouched), bias, all prologues, a full-size
 bank with sampled rows, and a CUDA graph replayed after the routing changes.
+A token's outputs do not depend on the other tokens or their routing: each
+token of an 8-token call equals that token run alone (bit for bit; a
+one-token launch runs the kernel compiled for one row).
 """
 import numpy as np
 import pytest
@@ -47,6 +50,8 @@ def _oracle(c, E, N, ids, bias=None, rows=None):
     ("w6a8", "swiglu", 8, 4, 128, 160, 32, 3),
     ("w4a8", "none", 1, 9, 384, 1056, 32, 4),
     ("w4a8", "rmsnorm", 8, 5, 128, 512, 64, 8),
+    ("w4a8", "rmsnorm", 1, 17, 256, 1280, 128, 8),
+    ("w6a8", "swiglu", 1, 6, 128, 512, 32, 2),
 ])
 def test_moe_matches_oracle(fmt, kind, M, E, N, K, G, topk):
     c, w = _bank(fmt, kind, M, E, N, K, G, seed=E * N + K + topk)
@@ -114,3 +119,22 @@ def test_moe_graph_follows_device_routing():
         ref = _oracle(c, E, N, np.array(route))
         assert_y_close(y.cpu().numpy(), ref["y64"], f"route {route}")
     assert qlin.read_device_status(ws) == qlin.OK
+
+
+@pytest.mark.parametrize("fmt,kind,G", [("w4a8", "rmsnorm", 128), ("w4a8", "swiglu", 64), ("w6a8", "none", 32)])
+def test_moe_token_alone_equals_token_in_batch(fmt, kind, G):
+    """Each token of an 8-token call, bit for bit, against the same token run
+    alone (a one-token launch), with the same routing for that token."""
+    M, E, N, K, topk = 8, 12, 256, 2048, 3
+    c, w = _bank(fmt, kind, M, E, N, K, G, seed=17 + G)
+    rng = np.random.default_rng(G)
+    ids = np.stack([rng.choice(E, size=topk, replace=False) for _ in range(M)]).astype(np.int32)
+    a = _acts_dev(c)
+    y8 = qlin.forward_moe(fmt, kind, w, E, N, K, G, torch.from_numpy(ids).to(DEV), eps=c.eps, flags=qlin.FLAG_PDL, **a)
+    for m in range(M):
+        one = {k: (v[m:m + 1].contiguous() if k in ("x", "gate", "up") and v is not None else v) for k, v in a.items()}
+        y1 = qlin.forward_moe(fmt, kind, w, E, N, K, G, torch.from_numpy(ids[m:m + 1].copy()).to(DEV), eps=c.eps,
+                              flags=qlin.FLAG_PDL, **one)
+        assert torch.equal(y1[0], y8[m]), m
+    ref = _oracle(c, E, N, ids)
+    assert_y_close(y8.cpu().numpy(), ref["y64"], f"{fmt} {kind} bank")

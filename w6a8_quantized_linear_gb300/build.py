@@ -20,7 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libqlin.so")
 UNITS = ["qlin_api.cu", "qlin_kernels_w4.cu", "qlin_kernels_w6.cu", "qlin_kernels_codebook.cu",
          "qlin_kernels_moe_w4.cu", "qlin_kernels_moe_w6.cu", "qlin_kernels_export_w4.cu", "qlin_kernels_export_w6.cu",
-         "qlin_kernels_tc.cu", "qlin_kernels_tc_export.cu", "qlin_kernels_w4_one_row.cu", "qlin_kernels_w6_one_row.cu"]
+         "qlin_kernels_tc.cu", "qlin_kernels_tc_export.cu", "qlin_kernels_w4_one_row.cu", "qlin_kernels_w6_one_row.cu",
+         "qlin_kernels_moe_one_row.cu", "qlin_kernels_codebook_one_row.cu"]
 SOURCES = [os.path.join(CSRC, f) for f in UNITS + ["qlin_forward.cuh", "qlin_forward_tc.cuh", "qlin_repack.cuh", "qlin_layout.h",
                                                    "qlin_ptx.cuh", "qlin_instances.h"]] + [
     os.path.join(INCLUDE, "qlin.h")]

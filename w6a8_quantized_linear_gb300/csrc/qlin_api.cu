@@ -78,12 +78,12 @@ const void* fwd_fn() {
   return reinterpret_cast<const void*>(qlin_forward_kernel<BITS, G, MODE>);
 }
 // Kernels by group size index: 32, 64, 128, 256, 16, 8, 4.  Expert banks
-// (mode 1) and codebooks (mode 2, 4-bit codes) are built for G >= 32, the
-// plain modes (0, and 3 with the test exports) for every G; groups of 8 and
-// 4 exist for 4-bit codes only.
+// (modes 1 and 5) and codebooks (modes 2 and 6, 4-bit codes) are built for
+// G >= 32, the plain modes (0, 3 with the test exports, 4 for one row) for
+// every G; groups of 8 and 4 exist for 4-bit codes only.
 template <int BITS, int MODE>
 const void* fwd_fn_g(int gi) {
-  if constexpr (MODE == 2 && BITS != 4) return nullptr;
+  if constexpr ((MODE == 2 || MODE == 6) && BITS != 4) return nullptr;
   else {
     switch (gi) {
       case 0: return fwd_fn<BITS, 32, MODE>();
@@ -117,6 +117,8 @@ const void* forward_fn(int bits, int64_t G, int mode = 0) {
          : mode == 2 ? forward_fn_t<2>(bits, G)
          : mode == 3 ? forward_fn_t<3>(bits, G)
          : mode == 4 ? forward_fn_t<4>(bits, G)
+         : mode == 5 ? forward_fn_t<5>(bits, G)
+         : mode == 6 ? forward_fn_t<6>(bits, G)
                      : forward_fn_t<0>(bits, G);
 }
 
@@ -151,7 +153,7 @@ qlin_status device_cache(DevCache** out) {
     if (e != cudaSuccess) return cuda_status(e);
     for (int bits : {4, 6})
       for (int64_t G : {4, 8, 16, 32, 64, 128, 256})
-        for (int mode = 0; mode < 5; mode++) {
+        for (int mode = 0; mode < 7; mode++) {
           const void* fn = forward_fn(bits, G, mode);
           if (!fn) continue;
           e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_MAX);
@@ -390,9 +392,10 @@ qlin_status plan_and_launch(FwdParams& p, int fmt, int kind, int M, int64_t K, i
   p.fault_unit = fault_unit;
   p.f16_base = 0x64006400u;  // fp16 1024.0 in both halves
   void* args[] = {&p};
-  // one activation row on the plain weight table: the kernel without the
-  // code of the wider prologues (planned, above, as the plain kernel)
-  const int launch_mode = (mode == 0 && M == 1) ? 4 : mode;
+  // one activation row (plain table, expert bank or codebook): the kernel
+  // without the code of the wider prologues (planned, above, as the kernel
+  // of its mode)
+  const int launch_mode = (M == 1 && mode <= 2) ? 4 + mode : mode;
   return launch(tc ? tc_fn(g.bits, G, mode) : forward_fn(g.bits, G, launch_mode), dim3((unsigned)pl.C, (unsigned)pl.NB, 1),
                 dim3(tc ? TC_THREADS : GEMV_THREADS, 1, 1), (size_t)pl.smem, static_cast<cudaStream_t>(stream), args,
                 pl.C, (flags & QLIN_FLAG_PDL) != 0);

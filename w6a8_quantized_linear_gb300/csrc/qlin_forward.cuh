@@ -317,13 +317,14 @@ __device__ __forceinline__ void group_mma(const uint32_t (&a)[4], const uint32_t
 // MODE: 0 plain (weight table), 1 expert bank, 2 4-bit codebook levels,
 // 3 plain with the test hooks (activation codes, row scales and exact group
 // sums exported; one weight copy withheld), kept out of the other modes so
-// that their hot code stays compact; 4 plain for one activation row only (the
-// decode step without drafts: its launches then carry none of the code of
-// the 2-, 4- and 8-row prologues, which costs a step measurably even when it
-// never runs).  Mode 4 computes exactly what mode 0 computes for M = 1.
+// that their hot code stays compact; 4, 5 and 6 the plain, expert-bank and
+// codebook modes for one activation row only (the decode step without
+// drafts: its launches then carry none of the code of the 2-, 4- and 8-row
+// prologues, which costs a step measurably even when it never runs).  Modes
+// 4, 5 and 6 compute exactly what modes 0, 1 and 2 compute for M = 1.
 template <int BITS, int G, int MODE>
 __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams p) {
-  constexpr bool MOE = MODE == 1, CB = MODE == 2, EXPORT = MODE == 3, ONE_ROW = MODE == 4;
+  constexpr bool MOE = MODE == 1 || MODE == 5, CB = MODE == 2 || MODE == 6, EXPORT = MODE == 3, ONE_ROW = MODE >= 4;
   // dynamic shared memory: [codebook table (codebook mode)][stages][activation
   // operand][split-K slots]; the table sits first so that its address is a
   // constant of the kernel

@@ -1,11 +1,12 @@
 // The forward-kernel variants this library builds: X(BITS, G, MODE) for every
 // group size the format allows (4 and 8 for 4-bit codes only) in mode 0
 // (plain weight table), mode 3 (the same with the test exports) and mode 4
-// (the same for one activation row), G >= 32 for expert banks (mode 1), and
-// 4-bit codes with G >= 32 for codebook levels (mode 2).  The prologue kind is a runtime
-// parameter, so consecutive launches of different prologues run the same
-// code.  The variants are instantiated in seven translation units (compiled
-// in parallel) and declared extern where the host code takes their addresses.
+// (the same for one activation row), G >= 32 for expert banks (modes 1 and 5,
+// the latter for one row), and 4-bit codes with G >= 32 for codebook levels
+// (modes 2 and 6).  The prologue kind is a runtime parameter, so consecutive
+// launches of different prologues run the same code.  The variants are
+// instantiated in several translation units (compiled in parallel) and
+// declared extern where the host code takes their addresses.
 #pragma once
 
 #define QLIN_KERNELS_W4(X) X(4, 4, 0) X(4, 8, 0) X(4, 16, 0) X(4, 32, 0) X(4, 64, 0) X(4, 128, 0) X(4, 256, 0)
@@ -18,9 +19,14 @@
 // mode 4: the plain weight table for one activation row
 #define QLIN_KERNELS_ONE_ROW_W4(X) X(4, 4, 4) X(4, 8, 4) X(4, 16, 4) X(4, 32, 4) X(4, 64, 4) X(4, 128, 4) X(4, 256, 4)
 #define QLIN_KERNELS_ONE_ROW_W6(X) X(6, 16, 4) X(6, 32, 4) X(6, 64, 4) X(6, 128, 4) X(6, 256, 4)
+// modes 5 and 6: expert banks and codebook levels for one activation row
+#define QLIN_KERNELS_MOE_ONE_ROW(X) \
+  X(4, 32, 5) X(4, 64, 5) X(4, 128, 5) X(4, 256, 5) X(6, 32, 5) X(6, 64, 5) X(6, 128, 5) X(6, 256, 5)
+#define QLIN_KERNELS_CODEBOOK_ONE_ROW(X) X(4, 32, 6) X(4, 64, 6) X(4, 128, 6) X(4, 256, 6)
 #define QLIN_KERNELS_ALL(X)                                                                                 \
   QLIN_KERNELS_W4(X) QLIN_KERNELS_W6(X) QLIN_KERNELS_CODEBOOK(X) QLIN_KERNELS_MOE_W4(X) QLIN_KERNELS_MOE_W6(X) \
-  QLIN_KERNELS_EXPORT_W4(X) QLIN_KERNELS_EXPORT_W6(X) QLIN_KERNELS_ONE_ROW_W4(X) QLIN_KERNELS_ONE_ROW_W6(X)
+  QLIN_KERNELS_EXPORT_W4(X) QLIN_KERNELS_EXPORT_W6(X) QLIN_KERNELS_ONE_ROW_W4(X) QLIN_KERNELS_ONE_ROW_W6(X)   \
+  QLIN_KERNELS_MOE_ONE_ROW(X) QLIN_KERNELS_CODEBOOK_ONE_ROW(X)
 
 // The tcgen05 main loop (qlin_tc_kernel): groups of 32 k and more, the weight
 // table without (mode 0) and with (mode 3) the test hooks.
