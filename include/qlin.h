@@ -44,7 +44,8 @@
  *  - fmt is QLIN_W4A8 or QLIN_W6A8; b = 4 or 6 bits per code.
  *  - Backend limits beyond [OPT] (QLIN_ERR_UNSUPPORTED): G in {4, 8, 16, 32,
  *    64, 128, 256} (4 and 8 for 4-bit codes, as the format allows),
- *    K % 32 == 0, N % 16 == 0, K <= 65536, M <= 8.
+ *    K % 32 == 0, N % 16 == 0, K <= 65536 (K <= 57344 for G = 4, whose
+ *    per-group start values fill the shared memory of 16 CTAs first), M <= 8.
  */
 #ifndef QLIN_H_
 #define QLIN_H_
@@ -162,7 +163,9 @@ qlin_status qlin_workspace_init(void* ws, size_t ws_bytes, void* stream);
 /*
  * y = packed-weight x quantised activation [LIN], [ACT], [MTP].
  *   fmt, prologue : qlin_format, qlin_prologue.
- *   M             : rows, 1..8 (M = 0 or N = 0 enqueues nothing).
+ *   M             : rows, 1..8 (M = 0 or N = 0 enqueues nothing; with M = 0
+ *                   the activation and output pointers are not read and may
+ *                   be null).
  *   packed        : device, repacked stream (qlin_repack), 16-byte aligned.
  *   x             : bf16 [M, K] row-major, 16-byte aligned (NONE, RMSNORM).
  *   gate, up      : bf16 [M, K] row-major, 16-byte aligned (SWIGLU).

@@ -95,6 +95,14 @@ def _fwd(L, **kw):
                           a["up"], a["gamma"], a["eps"], a["y"], a["ws"], a["wsb"], a["flags"], a["stream"])
 
 
+def test_forward_with_no_rows_reads_nothing(L):
+    # M = 0: nothing is enqueued, so null activation and output pointers are
+    # fine (an empty tensor may have no address); the shape is still checked
+    for pro in (0, 1, 2):
+        assert _fwd(L, pro=pro, M=0, x=None, y=None, ws=None) == qlin.OK
+    assert _fwd(L, M=0, x=None, K=40, G=8) == qlin.ERR_INVALID_ARG
+
+
 def test_forward_rejects_bad_arguments_before_launch(L):
     # none of these reach the GPU (pointer values are never dereferenced)
     assert _fwd(L, fmt=5) == qlin.ERR_INVALID_ARG

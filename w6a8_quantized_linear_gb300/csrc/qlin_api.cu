@@ -325,6 +325,7 @@ qlin_status check_act(int kind, int M, const void* x, const void* gate, const vo
   if (kind < 0 || kind > 2) return QLIN_ERR_INVALID_ARG;
   if (M < 0) return QLIN_ERR_INVALID_ARG;
   if (M > MAX_M) return QLIN_ERR_UNSUPPORTED;
+  if (M == 0) return QLIN_OK;  // no row is read (an empty tensor may have no address)
   if (kind == QLIN_PROLOGUE_SWIGLU) {
     if (!gate || !up || !aligned(gate, 16) || !aligned(up, 16)) return QLIN_ERR_INVALID_ARG;
   } else {
