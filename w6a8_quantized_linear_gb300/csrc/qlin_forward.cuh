@@ -121,6 +121,18 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 r, float (&v)[8]) {
   }
 }
 
+// 127 / a for a > 0, within an ulp of the correctly rounded quotient: a fast
+// reciprocal r, q = 127 r, then one Newton step on the residual 127 - a q
+// (exact in an fma), q + r (127 - a q).  With r within a few ulp of 1/a the
+// step leaves a relative error of order the square of r's, below the final
+// rounding.  (No division routine: its slow path took registers from the
+// rest of the kernel.)
+__device__ __forceinline__ float quotient_127(float a) {
+  const float r = __fdividef(1.0f, a);
+  const float q = 127.0f * r;
+  return __fmaf_rn(__fmaf_rn(-a, q, 127.0f), r, q);
+}
+
 // A compile-time integer as a value (to pick a specialisation of a generic
 // lambda).
 template <int K>
@@ -611,16 +623,41 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
       for (int r = 0; r < C; r++) st_async_f2(dsmem_addr_u32(local, r), a, q, dsmem_addr_u32(lbar, r));
     }
     if (!mbar_wait_cluster(&stat_bar, 0) && lane == 0) atomicExch(p.status, 4u);
+    // Row scale s and the factor c that maps a prologue value to its code.
+    // With no prologue s and the quotients are IEEE, so the codes equal the
+    // definition bit for bit; with a prologue the tolerance of the method
+    // allows a product by c, rounded once (see phase 2).  The code of value v
+    // is v * rstd / s = v * 127 / a: rstd cancels, so c = 127 / a, to within
+    // an ulp (codes then differ from the exact quotient only within about an
+    // ulp of a rounding boundary).
+    float s_one = 0.f, c_one = 0.f;
+    if constexpr (ONE_ROW) {
+      // one row: every thread forms s and c itself (the same sums in the same
+      // order), so phase 2 needs no barrier after them; thread 0 keeps s for
+      // the output
+      float a = 0.f, q = 0.f;
+      for (int r = 0; r < C; r++) {  // fixed rank order: the same sums in every CTA
+        a = fmaxf(a, s_slot[r][0][0]);
+        q = __fadd_rn(q, s_slot[r][0][1]);
+      }
+      if (KIND == 0) {
+        s_one = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
+      } else {
+        const float rs = KIND == 1 ? rsqrtf(__fadd_rn(__fmul_rn(q, p.inv_k), p.eps)) : 1.0f;
+        s_one = __fmul_rn(a, rs) * (1.0f / 127.0f);
+        c_one = a > 0.f ? quotient_127(a) : 0.f;
+      }
+      if (tid == 0) {
+        s_row[0][0] = s_one;
+        s_row[0][1] = c_one;
+      }
+    } else {
     if (tid < M) {
       float a = 0.f, q = 0.f;
       for (int r = 0; r < C; r++) {  // fixed rank order: the same sums in every CTA
         a = fmaxf(a, s_slot[r][tid][0]);
         q = __fadd_rn(q, s_slot[r][tid][1]);
       }
-      // Row scale s and the factor c that maps a prologue value to its code.
-      // With no prologue s and the quotients are IEEE, so the codes equal the
-      // definition bit for bit; with a prologue the tolerance of the method
-      // allows a product by c, rounded once (see phase 2).
       float s, c;
       if (KIND == 0) {
         s = a > 0.f ? __fdiv_rn(a, 127.0f) : 0.f;
@@ -629,16 +666,14 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
         const float rs = KIND == 1 ? rsqrtf(__fadd_rn(__fmul_rn(q, p.inv_k), p.eps)) : 1.0f;
         const float amax = __fmul_rn(a, rs);  // = max |fl(x*gamma) * rstd| (rounding is monotone)
         s = amax * (1.0f / 127.0f);
-        // the code of value v is v * rstd / s = v * 127 / a: rstd cancels, so
-        // c = 127 / a, correctly rounded (codes then differ from the exact
-        // quotient only within about an ulp of a rounding boundary)
-        c = a > 0.f ? __fdiv_rn(127.0f, a) : 0.f;
+        c = a > 0.f ? quotient_127(a) : 0.f;
       }
       s_row[tid][0] = s;
       s_row[tid][1] = c;
       if (EXPORT && p.s_out && blockIdx.y == 0 && crank == 0) p.s_out[tid] = s;
     }
     consumer_bar();
+    }
 
     // ---- phase 2: quantise this CTA's K range into the MMA B operand (fp16),
     //      plus each sub-group's chain start values.  Every block is written
@@ -676,7 +711,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
               } else {
                 act.value(m, v, ss);
               }
-              const float s = s_row[m][0], c = s_row[m][1];
+              const float s = ONE_ROW ? s_one : s_row[m][0], c = ONE_ROW ? c_one : s_row[m][1];
               // |t| <= 127 (1 + a few ulp) because |a| <= amax, so round half to
               // even never leaves [-127, 127]: no clamp is needed
   #pragma unroll

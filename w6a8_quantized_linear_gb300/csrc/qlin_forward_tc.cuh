@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) qlin_tc_kernel(FwdParams p) {
         const float rs = KIND == 1 ? rsqrtf(__fadd_rn(__fmul_rn(q, p.inv_k), p.eps)) : 1.0f;
         const float amax = __fmul_rn(a, rs);
         s = amax * (1.0f / 127.0f);
-        c = a > 0.f ? __fdiv_rn(127.0f, a) : 0.f;  // rstd cancels from v * rstd / s (as in qlin_forward_kernel)
+        c = a > 0.f ? quotient_127(a) : 0.f;  // rstd cancels from v * rstd / s (as in qlin_forward_kernel)
       }
       s_row[tid][0] = s;
       s_row[tid][1] = c;
