@@ -158,6 +158,7 @@ TRAFFIC = {
     "0f3f5b1ea3945020": {"bytes_per_launch": 97141248},
     "2c2b2c737308ed6d": {"bytes_per_launch": 97567488},
     "2e15078fe7a49fc1": {"bytes_per_launch": 97483776},
+    "83ebf4d3cc1dcf8a": {"bytes_per_launch": 97519616},
 }
 TRAFFIC_METRICS = "ncu dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch"
 
