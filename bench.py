@@ -155,20 +155,24 @@ def max_over_ranks(v: float, ws: int, device) -> float:
 # kernel reports no traffic until it is captured again.
 KERNEL_SOURCES = ("qlin_forward.cuh", "qlin_ptx.cuh", "qlin_layout.h")
 TRAFFIC = {
-    "0f3f5b1ea3945020": {"bytes_per_launch": 97141248},
-    "2c2b2c737308ed6d": {"bytes_per_launch": 97567488},
-    "2e15078fe7a49fc1": {"bytes_per_launch": 97483776},
-    "83ebf4d3cc1dcf8a": {"bytes_per_launch": 97519616},
+    "245efc03d326fc99": {"bytes_per_launch": 97519616},
 }
 TRAFFIC_METRICS = "ncu dram__bytes_read.sum + dram__bytes_write.sum of one gate/up launch"
 
 
 def kernel_hash() -> str:
+    """Hash of the kernel's code: the sources with comments removed and white
+    space collapsed, so that a comment edit keeps a capture's counters valid
+    (the sources hold no comment markers inside string literals)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "w6a8_quantized_linear_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "w6a8_quantized_linear_gb300", "csrc", f), encoding="utf-8") as fh:
+            code = fh.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -47,5 +47,21 @@ def test_traffic_is_keyed_by_the_kernel_sources(monkeypatch):
     assert bench.kernel_traffic() is None
 
 
+def test_kernel_hash_follows_code_not_comments(monkeypatch, tmp_path):
+    import shutil
+    src = os.path.join(ROOT, "w6a8_quantized_linear_gb300", "csrc")
+    dst = tmp_path / "w6a8_quantized_linear_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for f in bench.KERNEL_SOURCES:
+        shutil.copy(os.path.join(src, f), dst / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_hash()
+    k = dst / "qlin_layout.h"
+    k.write_text(k.read_text() + "\n// a remark\n/* another\n   remark */\n")
+    assert bench.kernel_hash() == h0
+    k.write_text(k.read_text() + "\nconstexpr int qlin_unused_constant = 1;\n")
+    assert bench.kernel_hash() != h0
+
+
 def test_job_throughput_is_total_bytes_over_slowest_rank():
     assert abs(bench.job_gbs(4, 10**9, 2.0) - 2000.0) < 1e-9

@@ -24,14 +24,16 @@
 // kernel reads them; the M <= 8 rows sit on the 8-wide side of the MMA).
 //
 // Variants.  The kernel is compiled per code width, group size and mode
-// (plain weight table, expert bank, codebook levels, plain with test hooks).
+// (plain weight table, expert bank, codebook levels, plain with test hooks,
+// and the plain, expert-bank and codebook modes for one activation row).
 // The prologue kind (none, RMSNorm, SwiGLU) and the rows (at most 1, 2, 4 or
 // 8) are launch parameters: the CTA branches once to a prologue compiled for
 // them, so the launches of a layer run the same main-loop code and a short
 // launch carries only the registers and code of the rows it has.  Code that
 // a launch never runs still costs it (instruction fetch and register
 // allocation of once-per-CTA phases), which is why the test hooks are a mode
-// of their own.
+// of their own and a one-row launch (the host picks it at M = 1) runs a
+// kernel with the one-row prologue only.
 //
 // Exactness of the fp16 positional route.  fp16 1024.0 (0x6400) has ten
 // mantissa bits of weight 1, 2, ..., 512.  A code c (0 <= c < 64) ORed into
