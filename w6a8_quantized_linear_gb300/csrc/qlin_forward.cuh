@@ -395,61 +395,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
     }
   }
   if constexpr (MOE) {
-    __shared__ uint32_t s_ebits[MOE_MAX_E / 32];  // routed experts
-    __shared__ int s_expert;
-    // Expert bank: the routing comes from an earlier kernel, so nothing is
-    // read before the dependency wait.  The routed experts, in increasing
-    // id, take the row-block slots in order; a slot past the last routed
-    // expert has no work, and its whole cluster (same blockIdx.y) leaves
-    // here, before any barrier or shared-memory exchange.
-    pdl_wait();
-    const int nid = p.M * p.topk;
-    const int my_id = tid < nid ? p.ids[tid] : -1;  // in flight while the bitmap is cleared
-    for (int w = tid; w < MOE_MAX_E / 32; w += GEMV_THREADS) s_ebits[w] = 0u;
-    if (tid == 0) s_expert = -1;
-    if (tid < MAX_M) s_tokmask[tid] = 0u;
-    __syncthreads();
-    if (my_id >= 0 && my_id < p.E) atomicOr(&s_ebits[my_id >> 5], 1u << (my_id & 31));
-    __syncthreads();
-    if (warp == 0) {
-      constexpr int WPL = MOE_MAX_E / 32 / 32;  // bitmap words per lane
-      uint32_t wd[WPL];
-      int cnt = 0;
-#pragma unroll
-      for (int i = 0; i < WPL; i++) {
-        wd[i] = s_ebits[lane * WPL + i];
-        cnt += __popc(wd[i]);
-      }
-      int incl = cnt;  // inclusive prefix of the counts over the lanes
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const int a = (int)(blockIdx.y / p.nbe);
-      int r = a - (incl - cnt);
-      if (r >= 0 && r < cnt) {
-#pragma unroll
-        for (int i = 0; i < WPL; i++) {
-          const int pc = __popc(wd[i]);
-          if (r >= 0 && r < pc) {
-            uint32_t v = wd[i];
-            for (int k = 0; k < r; k++) v &= v - 1u;  // drop the r lowest set bits
-            s_expert = (lane * WPL + i) * 32 + (__ffs(v) - 1);
-          }
-          r -= pc;
-        }
-      }
-    }
-    __syncthreads();
-    const int expert = s_expert;
-    if (expert < 0) return;
-    // the slots of each token routed here, from the ids already in registers
-    // (visible to every thread after the barrier initialisation's __syncthreads)
-    if (tid < nid && my_id == expert) atomicOr(&s_tokmask[tid / p.topk], 1u << (tid % p.topk));
-    packed = p.bank + (int64_t)expert * (p.ne / TILE_N) * p.tile_full;
+    // Expert bank: every expert has the same rows, so everything but the
+    // routed expert's weights and bias is known before the routing (below).
     y = p.ymoe;
-    bias = p.bank_bias ? p.bank_bias + (int64_t)expert * p.ne : nullptr;
     N = p.ne;
     T = p.ne / TILE_N;
     blk_first = (int64_t)(blockIdx.y / p.nbe) * p.nbe;
@@ -504,7 +452,68 @@ __global__ void __launch_bounds__(GEMV_THREADS, 2) qlin_forward_kernel(FwdParams
   }
   __syncthreads();
   cluster_arrive_relaxed();  // peers may push into this CTA once every CTA has passed here
-  pdl_launch_dependents();
+  // (an expert bank lets the next launch in after its routing, as it measured
+  // faster: earlier, the next launch's CTAs took slots this launch's slow
+  // tail then shared)
+  if constexpr (!MOE) pdl_launch_dependents();
+  if constexpr (MOE) {
+    __shared__ uint32_t s_ebits[MOE_MAX_E / 32];  // routed experts
+    __shared__ int s_expert;
+    // Expert bank: the routing comes from an earlier kernel, so nothing is
+    // read before the dependency wait; the CTA sets up its barriers first.
+    // The routed experts, in increasing id, take the row-block slots in
+    // order; a slot past the last routed expert has no work, and its whole
+    // cluster (same blockIdx.y) leaves here, before any wait on a barrier or
+    // shared-memory exchange.
+    pdl_wait();
+    const int nid = p.M * p.topk;
+    const int my_id = tid < nid ? p.ids[tid] : -1;  // in flight while the bitmap is cleared
+    for (int w = tid; w < MOE_MAX_E / 32; w += GEMV_THREADS) s_ebits[w] = 0u;
+    if (tid == 0) s_expert = -1;
+    if (tid < MAX_M) s_tokmask[tid] = 0u;
+    __syncthreads();
+    if (my_id >= 0 && my_id < p.E) atomicOr(&s_ebits[my_id >> 5], 1u << (my_id & 31));
+    __syncthreads();
+    if (warp == 0) {
+      constexpr int WPL = MOE_MAX_E / 32 / 32;  // bitmap words per lane
+      uint32_t wd[WPL];
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < WPL; i++) {
+        wd[i] = s_ebits[lane * WPL + i];
+        cnt += __popc(wd[i]);
+      }
+      int incl = cnt;  // inclusive prefix of the counts over the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int a = (int)(blockIdx.y / p.nbe);
+      int r = a - (incl - cnt);
+      if (r >= 0 && r < cnt) {
+#pragma unroll
+        for (int i = 0; i < WPL; i++) {
+          const int pc = __popc(wd[i]);
+          if (r >= 0 && r < pc) {
+            uint32_t v = wd[i];
+            for (int k = 0; k < r; k++) v &= v - 1u;  // drop the r lowest set bits
+            s_expert = (lane * WPL + i) * 32 + (__ffs(v) - 1);
+          }
+          r -= pc;
+        }
+      }
+    }
+    __syncthreads();
+    const int expert = s_expert;
+    pdl_launch_dependents();
+    if (expert < 0) return;
+    // the slots of each token routed here, from the ids already in registers
+    // (read in the epilogue, after the consumers' later barriers)
+    if (tid < nid && my_id == expert) atomicOr(&s_tokmask[tid / p.topk], 1u << (tid % p.topk));
+    packed = p.bank + (int64_t)expert * (p.ne / TILE_N) * p.tile_full;
+    bias = p.bank_bias ? p.bank_bias + (int64_t)expert * p.ne : nullptr;
+  }
 
   if (warp == CONSUMER_WARPS) {
     // ------------------------------------------------------------------ producer
